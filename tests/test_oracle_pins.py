@@ -1,0 +1,332 @@
+"""Pins of the float64 oracle to what the pages and the mathematics fix (CPU only).
+
+Each test ties the oracle to something other than itself: numbers printed on
+the pages (tests/golden/), closed forms proved there, library routines, or a
+black-box measurement of the oracle's own output law (tests/law.py) compared
+with the closed-form law of the A.1 argument.
+"""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle as O
+from law import all_small_cases, first_token_marginal, measure_law
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rows(name):
+    rows = []
+    for line in open(os.path.join(GOLDEN, name)):
+        line = line.split("#")[0].strip()
+        if line:
+            rows.append(line.split())
+    return rows
+
+
+def _run_row(tl, dl, ids, u):
+    return O.verify_row(tl, dl, ids, dl.shape[0], u, 1.0)
+
+
+# ----------------------------------------------------------------------------- exactness (A.1)
+
+@pytest.mark.parametrize("case", list(all_small_cases()), ids=lambda c: f"V{c[0]}g{c[1]}")
+def test_measured_law_equals_closed_form_joint(case):
+    """Brute force over V <= 4, gamma <= 2: the oracle's law equals the A.1 closed form."""
+    V, gamma, p, q = case
+    law = measure_law(_run_row, p, q)
+    exact = O.exact_joint(p, q)
+    keys = set(law) | set(exact)
+    err = max(abs(law.get(k, 0.0) - exact.get(k, 0.0)) for k in keys)
+    assert err < 1e-12, (err, law, exact)
+    assert abs(sum(law.values()) - 1.0) < 1e-12
+
+
+@pytest.mark.parametrize("case", list(all_small_cases(seed=11)), ids=lambda c: f"V{c[0]}g{c[1]}")
+def test_first_emitted_token_is_distributed_as_p1(case):
+    """The theorem the pages prove: the first emitted token has law p_1, whatever q is."""
+    V, gamma, p, q = case
+    law = measure_law(_run_row, p, q)
+    assert np.max(np.abs(first_token_marginal(law, V) - p[0])) < 1e-12
+
+
+def test_disjoint_support_draft_still_gives_p():
+    """Disjoint supports: nothing is ever accepted, beta = 0, and the emitted token still has law p."""
+    p = np.array([[0.5, 0.5, 0.0, 0.0], [0.25, 0.25, 0.25, 0.25]])
+    q = np.array([[0.0, 0.0, 0.3, 0.7]])
+    law = measure_law(_run_row, p, q)
+    assert all(len(k) == 1 for k in law)
+    assert np.max(np.abs(first_token_marginal(law, 4) - p[0])) < 1e-14
+    with np.errstate(divide="ignore"):
+        s = O.stats_position(np.log(p[0]), np.log(q[0]), 2, 1.0)
+    assert s["beta"] == 0.0 and abs(s["resid"] - 1.0) < 1e-15 and s["accept_prob"] == 0.0
+
+
+def test_identical_distributions_accept_everything():
+    """p == q: DLK = 0, beta = 1, every guess is accepted and the bonus comes from p_{gamma+1}."""
+    rng = np.random.default_rng(3)
+    p = rng.dirichlet(np.ones(3), size=3)
+    law = measure_law(_run_row, p, p[:2].copy())
+    assert all(len(k) == 3 for k in law)
+    s = O.stats_position(np.log(p[0]), np.log(p[0]), 1, 1.0)
+    assert s["beta"] == pytest.approx(1.0, abs=1e-15) and s["resid"] == 0.0 and s["accept_prob"] == 1.0
+
+
+# ----------------------------------------------------------------------------- acceptance rate (Thm 3.5)
+
+def test_acceptance_rate_is_overlap_and_one_minus_tv():
+    """Measured P(accept first guess) = sum min(p, q) = 1 - DLK = 1 - (1/2) sum |p - q|."""
+    rng = np.random.default_rng(5)
+    for V in (2, 3, 4):
+        for _ in range(5):
+            p = rng.dirichlet(np.ones(V), size=2)
+            q = rng.dirichlet(np.ones(V), size=1)
+            law = measure_law(_run_row, p, q)
+            accept = sum(v for k, v in law.items() if len(k) == 2)
+            s = O.stats_position(np.log(p[0]), np.log(q[0]), 0, 1.0)
+            tv = 0.5 * np.sum(np.abs(p[0] - q[0]))
+            mid = 0.5 * (p[0] + q[0])
+            dlk = np.sum(np.abs(p[0] - mid))          # Definition 3.2
+            assert accept == pytest.approx(s["beta"], abs=1e-12)
+            assert s["beta"] == pytest.approx(1.0 - tv, abs=1e-14)
+            assert s["beta"] == pytest.approx(1.0 - dlk, abs=1e-14)
+            assert s["resid"] == pytest.approx(tv, abs=1e-14)
+
+
+def test_per_position_accept_probability_is_min_one_ratio():
+    """Measured acceptance threshold of one draft = min(1, p(x)/q(x)) (Phase 3)."""
+    p = np.array([[0.1, 0.2, 0.3, 0.4], [0.25] * 4])
+    q = np.array([[0.4, 0.1, 0.3, 0.2]])
+    with np.errstate(divide="ignore"):
+        tl, dl = np.log(p), np.log(q)
+    for x in range(4):
+        lo, hi = 0.0, 1.0
+        for _ in range(60):
+            mid = 0.5 * (lo + hi)
+            n = O.verify_row(tl, dl, np.array([x]), 1, np.array([mid, 0.5]), 1.0)["n"]
+            lo, hi = (mid, hi) if n == 1 else (lo, mid)
+        assert lo == pytest.approx(min(1.0, p[0, x] / q[0, x]), abs=1e-12)
+
+
+def test_two_token_example():
+    rows = {r[0]: r[1:] for r in _rows("two_token_example.txt")}
+    p = np.array([[float(rows["A"][0]), float(rows["B"][0])], [0.5, 0.5]])
+    q = np.array([[float(rows["A"][1]), float(rows["B"][1])]])
+    law = measure_law(_run_row, p, q)
+    accept = sum(v for k, v in law.items() if len(k) == 2)
+    assert accept == pytest.approx(float(rows["acceptance"][0]), abs=1e-12)
+    corrected = {k: v for k, v in law.items() if len(k) == 1}
+    assert set(corrected) == {(0,)}                 # every rejection is corrected to A
+    assert np.max(np.abs(first_token_marginal(law, 2) - p[0])) < 1e-12
+
+
+# ----------------------------------------------------------------------------- E[# tokens] (Eq. 1)
+
+def _measured_expected_tokens(alpha, gamma):
+    """p_i = (alpha, 1 - alpha), q_i = one-hot(0): every guess is accepted with probability alpha."""
+    p = np.tile([alpha, 1.0 - alpha], (gamma + 1, 1))
+    q = np.tile([1.0, 0.0], (gamma, 1))
+    law = measure_law(_run_row, p, q)
+    return sum(len(k) * v for k, v in law.items())
+
+
+@pytest.mark.parametrize("row", _rows("expected_tokens.txt"), ids=lambda r: f"a{r[0]}g{r[1]}")
+def test_expected_tokens_match_pages(row):
+    alpha, gamma, printed = float(row[0]), int(row[1]), float(row[2])
+    e = _measured_expected_tokens(alpha, gamma)
+    assert e == pytest.approx(O.expected_tokens(alpha, gamma), abs=1e-12)
+    assert abs(e - printed) <= 0.005 + 1e-12
+
+
+def test_expected_tokens_alpha_08_gamma_4_is_33616():
+    assert _measured_expected_tokens(0.8, 4) == pytest.approx(3.3616, abs=1e-12)
+
+
+@pytest.mark.parametrize("row", _rows("table1_speed_ops.txt"), ids=lambda r: f"a{r[0]}g{r[1]}")
+def test_table1_speed_and_operations(row):
+    alpha, gamma, speed, ops = float(row[0]), int(row[1]), float(row[2]), float(row[3])
+    assert abs(O.walltime_improvement(alpha, gamma, 0.0) - speed) <= 0.005 + 1e-12
+    assert abs(O.operations_factor(alpha, gamma, 0.0) - ops) <= 0.005 + 1e-12
+    assert O.walltime_improvement(alpha, gamma, 0.0) == pytest.approx(_measured_expected_tokens(alpha, gamma),
+                                                                      abs=1e-12)
+
+
+@pytest.mark.parametrize("row", _rows("speedup_examples.txt"), ids=lambda r: f"a{r[0]}g{r[1]}c{r[2]}")
+def test_speedup_examples(row):
+    alpha, gamma, c, printed, dec = float(row[0]), int(row[1]), float(row[2]), float(row[3]), int(row[4])
+    assert abs(O.walltime_improvement(alpha, gamma, c) - printed) <= 0.5 * 10 ** -dec + 1e-12
+
+
+# ----------------------------------------------------------------------------- standardisation
+
+def test_softmax_matches_scipy():
+    rng = np.random.default_rng(0)
+    for T in (0.3, 0.7, 1.0, 2.5):
+        l = rng.normal(0, 4, size=1000)
+        l[::17] = -np.inf
+        np.testing.assert_allclose(O.softmax_t(l, T), scipy.special.softmax(l / T), rtol=1e-13, atol=0)
+
+
+def test_bf16_widening_matches_torch_on_every_bit_pattern():
+    bits = np.arange(65536, dtype=np.uint16)
+    ours = O.widen(bits, "bf16")
+    ref = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+    same = (ours == ref) | (np.isnan(ours) & np.isnan(ref))
+    assert same.all()
+
+
+def test_greedy_is_sampling_with_one_hot_standardisation():
+    """Argmax standardisation: greedy verification equals sampling with one-hot p and q."""
+    rng = np.random.default_rng(9)
+    for trial in range(200):
+        V, gamma = int(rng.integers(2, 9)), int(rng.integers(0, 5))
+        tl = np.round(rng.normal(0, 1, size=(gamma + 1, V)), 1)   # rounding makes ties common
+        dl = np.where(rng.random((gamma, V)) < 0.5, tl[:gamma], rng.normal(0, 1, size=(gamma, V)))
+        ids = np.array([int(np.argmax(d)) for d in dl], dtype=np.int64)
+        g = O.greedy_row(tl, ids, gamma, gamma)
+        with np.errstate(divide="ignore"):
+            tp = np.log(np.eye(V)[[int(np.argmax(t)) for t in tl]])
+            dq = np.log(np.eye(V)[ids]) if gamma else np.zeros((0, V))
+        u = rng.random(gamma + 1) * 0.999
+        s = O.verify_row(tp, dq, ids, gamma, u, 1.0)
+        assert s["emitted"] == g["emitted"] and s["n"] == g["n"]
+
+
+def test_greedy_lowest_index_tie_break():
+    tl = np.array([[1.0, 3.0, 3.0, 0.0], [5.0, 5.0, -np.inf, 5.0]])
+    g = O.greedy_row(tl, np.array([2]), 1, 1)
+    assert g["n"] == 0 and g["emitted"] == [1, -1]
+    g = O.greedy_row(tl, np.array([1]), 1, 1)
+    assert g["n"] == 1 and g["emitted"] == [1, 0]
+
+
+def test_temperature_zero_limit_of_sampling_is_greedy():
+    """As T -> 0 the temperature softmax tends to the argmax one-hot, so sampling tends to greedy."""
+    rng = np.random.default_rng(2)
+    for _ in range(50):
+        V, gamma = 6, 3
+        tl = rng.normal(0, 1, size=(gamma + 1, V))
+        dl = tl[:gamma] + rng.normal(0, 0.3, size=(gamma, V))
+        ids = np.argmax(dl, axis=1)
+        g = O.greedy_row(tl, ids, gamma, gamma)
+        s = O.verify_row(tl, dl, ids, gamma, np.full(gamma + 1, 0.5), 1e-3)
+        assert s["emitted"] == g["emitted"]
+
+
+# ----------------------------------------------------------------------------- inverse CDF, readings
+
+def test_inverse_cdf_gamma_zero_is_plain_sampling_from_p():
+    """gamma = 0 degenerates to one inverse-CDF draw from p_1: the measured law is p_1."""
+    p = np.array([[0.1, 0.0, 0.45, 0.45]])
+    law = measure_law(_run_row, p, np.zeros((0, 4)))
+    m = first_token_marginal(law, 4)
+    np.testing.assert_allclose(m, p[0], atol=1e-14)
+
+
+def test_inverse_cdf_picks_smallest_index_with_cdf_above_target():
+    w = np.array([0.0, 0.25, 0.0, 0.5, 0.25])
+    assert O.inverse_cdf(w, 0.0)[0] == 1
+    assert O.inverse_cdf(w, 0.3)[0] == 3
+    assert O.inverse_cdf(w, 0.9)[0] == 4
+    assert O.inverse_cdf(w, 0.999999999)[0] == 4
+    k, flag = O.inverse_cdf(w, 0.25)       # exactly on an edge: lands right of it, and is flagged
+    assert k == 3 and flag
+
+
+def test_boundary_flags():
+    p = np.array([[0.3, 0.7], [0.5, 0.5]])
+    q = np.array([[0.6, 0.4]])
+    tl, dl = np.log(p), np.log(q)
+    r = 0.5   # min(1, 0.3/0.6)
+    near = O.verify_row(tl, dl, np.array([0]), 1, np.array([r + 5e-6, 0.3]), 1.0)
+    far = O.verify_row(tl, dl, np.array([0]), 1, np.array([r + 5e-3, 0.3]), 1.0)
+    assert near["boundary"] and not far["boundary"]
+    # residual is (0, 0.3) normalised to (0, 1): u_f anywhere leads to token 1; edges at 0 and 1
+    assert far["emitted"] == [1, -1]
+    edge = O.verify_row(tl, dl, np.array([0]), 1, np.array([r + 5e-3, 2e-6]), 1.0)
+    assert edge["boundary"]
+
+
+def test_degenerate_residual_falls_back_to_p():
+    """R4: residual mass <= 1e-15 -> draw from p [interactiveml correction distribution]."""
+    tl = np.log(np.array([[0.5, 0.5], [0.5, 0.5]]))
+    dl = tl[:1] + np.array([[1e-15, 0.0]])     # q(0) exceeds p(0) by ~2.5e-16: Z ~ 2.5e-16
+    s = O.stats_position(tl[0], dl[0], 0, 1.0)
+    assert 0.0 < s["resid"] <= O.Z_FLOOR and s["accept_prob"] < 1.0
+    u_reject = float(np.nextafter(1.0, 0.0))
+    # the residual alone would put all its mass on token 1; the fallback to p sends u_f = 0.25 to token 0
+    s = O.verify_row(tl, dl, np.array([0]), 1, np.array([u_reject, 0.25]), 1.0)
+    assert s["n"] == 0 and s["emitted"] == [0, -1]
+
+
+def test_zero_probability_draft_never_accepted():
+    tl = np.log(np.array([[0.0, 1.0], [0.5, 0.5]]))
+    dl = np.log(np.array([[0.0, 1.0]]))
+    s = O.verify_row(tl, dl, np.array([0]), 1, np.array([0.0, 0.5]), 1.0)
+    assert s["n"] == 0 and s["emitted"] == [1, -1]
+
+
+def test_invalid_rows_and_ignored_padding():
+    V, gamma = 5, 3
+    rng = np.random.default_rng(1)
+    tl = rng.normal(size=(gamma + 1, V))
+    dl = rng.normal(size=(gamma, V))
+    ids = np.array([1, 2, 3])
+    u = np.array([0.1, 0.2, 0.3, 0.4])
+    assert O.verify_row(tl, dl, ids, gamma, u, 1.0)["valid"]
+    for mutate in ("nan", "posinf", "allneg", "id", "u", "ulast", "len"):
+        t, d, x, uu, gb = tl.copy(), dl.copy(), ids.copy(), u.copy(), gamma
+        if mutate == "nan":
+            t[1, 2] = np.nan
+        elif mutate == "posinf":
+            d[0, 0] = np.inf
+        elif mutate == "allneg":
+            t[3] = -np.inf
+        elif mutate == "id":
+            x[1] = V
+        elif mutate == "u":
+            uu[0] = 1.0
+        elif mutate == "ulast":
+            uu[gamma] = -0.1
+        elif mutate == "len":
+            gb = gamma + 1
+        r = O.verify_row(t, d, x, gb, uu, 1.0)
+        assert not r["valid"] and r["n"] == -1 and r["emitted"] == [-1] * (gamma + 1), mutate
+    # ragged row of length 1: padded rows, ids and uniforms are never read
+    t, d, x, uu = tl.copy(), dl.copy(), ids.copy(), u.copy()
+    t[2:] = np.nan
+    d[1:] = np.nan
+    x[1:] = -1
+    uu[1:gamma] = np.nan
+    r = O.verify_row(t, d, x, 1, uu, 1.0)
+    assert r["valid"] and 0 <= r["n"] <= 1 and r["emitted"][r["n"] + 1:] == [-1] * (gamma - r["n"])
+
+
+def test_batched_wrappers_match_rows():
+    rng = np.random.default_rng(4)
+    B, gamma, V = 6, 3, 17
+    t = rng.normal(size=(B, gamma + 1, V)).astype(np.float32)
+    d = (t[:, :gamma] + rng.normal(size=(B, gamma, V))).astype(np.float32)
+    ids = rng.integers(0, V, size=(B, gamma)).astype(np.int32)
+    gl = np.array([3, 0, 1, 2, 3, 3], dtype=np.int32)
+    u = rng.random((B, gamma + 1)).astype(np.float32)
+    out = O.verify_sample(t, d, "f32", ids, gl, u, 0.9)
+    for b in range(B):
+        r = O.verify_row(t[b].astype(np.float64), d[b].astype(np.float64), ids[b], int(gl[b]),
+                         u[b].astype(np.float64), float(np.float32(0.9)))
+        assert list(out["emitted"][b]) == r["emitted"] and out["n_accepted"][b] == r["n"]
+    g = O.verify_greedy(t, "f32", ids, gl)
+    st = O.accept_stats(t, d, "f32", ids, gl, 0.9)
+    for b in range(B):
+        r = O.greedy_row(t[b].astype(np.float64), ids[b], int(gl[b]), gamma)
+        assert list(g["emitted"][b]) == r["emitted"]
+        for i in range(gamma):
+            if i < gl[b]:
+                assert np.isfinite(st["beta"][b, i])
+            else:
+                assert np.isnan(st["beta"][b, i])
