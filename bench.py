@@ -1,0 +1,428 @@
+"""Throughput of the batched speculative-sampling verification step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload c3]
+
+A step is one spec_verify_sample call (accept test, first rejection, residual
+/ bonus inverse-CDF draw; every row of the hot path) over one batch of the
+seeded synthetic workload, inputs resident in HBM.  The default workload is c3
+(B=256, gamma=5, V=152064, fp32 logits, T=0.7): 1.71 GB of logits per call,
+13x the L2, so no flush is needed between calls.  Prints one JSON line.
+
+--impl reference times the float64 CPU oracle (the reference implementation
+of the method for this build) on the same workload and metric, over a bounded
+sample of rows per step.  Under torchrun each rank runs its own replica of the
+workload on its own GPU (no data-path collective); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+METRIC = "verified draft positions/sec"
+UNIT = "positions/s"
+
+
+# ----------------------------------------------------------------------------- ranks
+
+def dist_init():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 1, None
+    import torch.distributed as dist
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    if torch.cuda.is_available():
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    dist.init_process_group(backend=backend)
+    return dist.get_rank(), ws, dist
+
+
+def combine_ranks(elapsed_s: float, units: float, dist, device=None):
+    """Max elapsed time and total units over ranks (the whole-job aggregate)."""
+    if dist is None:
+        return elapsed_s, units
+    t = torch.tensor([elapsed_s, units], dtype=torch.float64, device=device)
+    mx = t.clone()
+    dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    sm = t.clone()
+    dist.all_reduce(sm, op=dist.ReduceOp.SUM)
+    return float(mx[0]), float(sm[1])
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock, power and throttle reasons while the GPU is busy."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self) -> dict | None:
+        rows = []
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(f[1]), smax=float(f[2]), power=float(f[3]),
+                                 hw=f[5].lower() == "active", hwt=f[6].lower() == "active",
+                                 swt=f[7].lower() == "active", pcap=f[8].lower() == "active"))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            if r["hw"]:
+                reasons.add("hw_slowdown")
+            if r["hwt"]:
+                reasons.add("hw_thermal_slowdown")
+            if r["swt"]:
+                reasons.add("sw_thermal_slowdown")
+            if r["pcap"]:
+                reasons.add("sw_power_cap")
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["smax"] for r in rows),
+                "power_w_max": max(r["power"] for r in rows), "reasons": sorted(reasons), "samples": len(rows),
+                "window": "timed region plus about 1 s of untimed calls before it"}
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def hbm_peak():
+    try:
+        with open(PEAKS_FILE) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sources_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_verification_40_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current kernel sources."""
+    try:
+        kv = {}
+        with open(TRAFFIC_FILE) as f:
+            for ln in f:
+                if ":" in ln and not ln.startswith("#"):
+                    k, v = ln.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("sources_digest") != kernel_sources_digest():
+            return None
+        return float(kv[f"{workload}_bytes_per_launch"])
+    except (OSError, ValueError, KeyError):
+        return None
+
+
+def workload_desc(w: W.Workload) -> dict:
+    return {"workload": f"{w.name}: {w.meta['desc']}", "B": w.B, "gamma": w.gamma, "V": w.V,
+            "logits": "fp32" if w.dtype == "f32" else "bf16", "T": w.T, "positions_per_step": w.positions(),
+            "read_once_bytes_per_step": w.read_once_bytes()}
+
+
+def time_device(fn, steps: int, warmup: int, stream):
+    """Average device milliseconds per call: CUDA events on the launching stream."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def oracle_pool(procs: int):
+    """Process pool for the oracle, started with spawn (safe after CUDA initialisation)."""
+    import multiprocessing as mp
+    return mp.get_context("spawn").Pool(procs)
+
+
+def _oracle_rows(args):
+    import oracle as O
+    target, draft, dtype, ids, gl, u, T = args
+    O.verify_sample(target, draft, dtype, ids, gl, u, T)
+    return target.shape[0]
+
+
+def cpu_oracle_rate(w: W.Workload, rows: int, procs: int, pool=None) -> dict:
+    """Oracle positions/s over the first `rows` rows (repeated over the batch as needed), on `procs` processes."""
+    h = {"target": W.logits_as_numpy(w.target), "draft": W.logits_as_numpy(w.draft),
+         "ids": w.ids.cpu().numpy(), "gl": None if w.draft_len is None else w.draft_len.cpu().numpy(),
+         "u": w.uniforms.cpu().numpy()}
+    idx = [r % w.B for r in range(rows)]
+    per = max(1, math.ceil(rows / max(1, procs)))
+    chunks = [idx[s:s + per] for s in range(0, rows, per)]
+    jobs = [(h["target"][c], h["draft"][c], w.dtype, h["ids"][c], None if h["gl"] is None else h["gl"][c],
+             h["u"][c], w.T) for c in chunks]
+    positions = sum(w.gamma if h["gl"] is None else int(h["gl"][r]) for r in idx)
+    if procs <= 1:
+        t0 = time.perf_counter()
+        for j in jobs:
+            _oracle_rows(j)
+        dt = time.perf_counter() - t0
+    elif pool is not None:
+        t0 = time.perf_counter()
+        pool.map(_oracle_rows, jobs)
+        dt = time.perf_counter() - t0
+    else:
+        with oracle_pool(procs) as pool:
+            pool.map(_oracle_rows, jobs[:procs])       # start-up and imports outside the timing
+            t0 = time.perf_counter()
+            pool.map(_oracle_rows, jobs)
+            dt = time.perf_counter() - t0
+    return {"value": positions / dt, "unit": UNIT, "cores": procs, "kind": "oracle",
+            "sample": f"{rows} rows of {w.name} (float64 numpy oracle, {positions} positions) in {dt:.2f} s"}
+
+
+# ----------------------------------------------------------------------------- arms
+
+def run_ours(a, rank, world, dist):
+    import speculative_decoding_verification_40_gb300 as S
+    dev = torch.device("cuda", torch.cuda.current_device())
+    k = int(a.workload.lstrip("c"))
+    w = W.make(k, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    pos = w.positions()
+    nbytes = w.read_once_bytes()
+    ws = S.workspace_for(dev, S.workspace_size(w.B, w.gamma, w.V, w.target.dtype))
+    em = torch.empty(w.B, w.gamma + 1, dtype=torch.int32, device=dev)
+    na = torch.empty(w.B, dtype=torch.int32, device=dev)
+
+    def step():
+        S.verify_sample(w.target, w.draft, w.ids, w.uniforms, w.T, w.draft_len, emitted=em, n_accepted=na,
+                        workspace=ws)
+
+    for _ in range(max(3, a.warmup)):
+        step()
+    torch.cuda.synchronize()
+    assert S.check_status(ws) == 0
+
+    with ClockSampler(dev.index) as clk:
+        # about 1 s of untimed calls so the clock samples see the GPU under this load
+        t_end = time.perf_counter() + 1.0
+        while time.perf_counter() < t_end:
+            for _ in range(20):
+                step()
+            torch.cuda.synchronize()
+        barrier(dist, dev)
+        torch.cuda.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(a.steps):
+            step()
+        end.record(stream)
+        torch.cuda.synchronize()
+        barrier(dist, dev)
+        elapsed = start.elapsed_time(end) / 1e3
+    clocks = clk.summary()
+    assert S.check_status(ws) == 0
+    t_max, units = combine_ranks(elapsed, float(pos * a.steps), dist, dev)
+    ms_per_step = elapsed * 1e3 / a.steps        # one launch per step: the kernel's average launch duration
+    achieved = nbytes / (ms_per_step * 1e-3) / 1e9
+    peak, peak_kind = hbm_peak()
+    traffic = recorded_traffic(w.name)
+
+    # end to end through the public API: pinned host inputs -> device -> verify -> host results
+    host = {n: getattr(w, n).cpu().pin_memory() for n in ("target", "draft", "ids", "uniforms")}
+    if w.draft_len is not None:
+        host["draft_len"] = w.draft_len.cpu().pin_memory()
+    dev_in = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
+    out_em = torch.empty(w.B, w.gamma + 1, dtype=torch.int32).pin_memory()
+    out_na = torch.empty(w.B, dtype=torch.int32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_em.numel() * 4 + out_na.numel() * 4
+
+    def e2e_step():
+        for n, t in host.items():
+            dev_in[n].copy_(t, non_blocking=True)
+        S.verify_sample(dev_in["target"], dev_in["draft"], dev_in["ids"], dev_in["uniforms"], w.T,
+                        dev_in.get("draft_len"), emitted=em, n_accepted=na, workspace=ws)
+        out_em.copy_(em, non_blocking=True)
+        out_na.copy_(na, non_blocking=True)
+
+    e2e_steps = max(3, min(a.steps, 20))
+    e2e_ms = time_device(e2e_step, e2e_steps, 2, stream)
+    assert S.check_status(ws) == 0
+    _, e2e_units = combine_ranks(e2e_ms, float(pos), dist, dev)
+
+    # the variants, one call each per step on the same batch (context for the line)
+    greedy_ms = time_device(lambda: S.verify_greedy(w.target, w.greedy_ids, w.draft_len, workspace=ws),
+                            max(10, a.steps), 3, stream)
+    stats_ms = time_device(lambda: S.accept_stats(w.target, w.draft, w.ids, w.T, w.draft_len, workspace=ws),
+                           max(10, a.steps), 3, stream)
+    esz = 4 if w.dtype == "f32" else 2
+    greedy_bytes = (w.B + pos) * w.V * esz          # target rows 0..gamma_b
+    stats_bytes = 2 * pos * w.V * esz               # target and draft rows 0..gamma_b-1
+    assert S.check_status(ws) == 0
+
+    also = {}
+    if not a.no_also:
+        for kk in (2, 4):
+            if kk == k:
+                continue
+            w2 = W.make(kk, device=dev)
+            ws2 = S.workspace_for(dev, S.workspace_size(w2.B, w2.gamma, w2.V, w2.target.dtype))
+            ms = time_device(lambda: S.verify_sample(w2.target, w2.draft, w2.ids, w2.uniforms, w2.T, w2.draft_len,
+                                                     workspace=ws2), max(20, a.steps), 5, stream)
+            gbs = w2.read_once_bytes() / (ms * 1e-3) / 1e9
+            also[w2.name] = {"ms_per_call": round(ms, 5), "positions_per_s": w2.positions() / (ms * 1e-3),
+                             "rows_per_s": w2.B / (ms * 1e-3), "GB_per_s": round(gbs, 1),
+                             "frac_of_measured_hbm": round(gbs / peak, 4)}
+            del w2
+        assert S.check_status(ws2) == 0
+
+    line = {
+        "metric": METRIC, "value": units / t_max, "unit": UNIT, "n_gpus": world, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded Philox workload, see workloads/)",
+        "config": {**workload_desc(w), "l2": "inputs larger than L2 (1.71 GB vs 129 MB); no flush",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "rows_per_s": w.B * a.steps * world / t_max,
+        "GB_per_s": achieved,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_kind": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "kernel": "verify_rows_kernel<float,false>",
+                     "algorithmic_bytes_per_launch": nbytes},
+        "e2e": {"value": e2e_units / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": a.steps,
+        "clocks": clocks,
+        "variants": {"greedy_ms_per_call": greedy_ms,
+                     "greedy_GB_per_s": greedy_bytes / (greedy_ms * 1e-3) / 1e9,
+                     "stats_ms_per_call": stats_ms,
+                     "stats_GB_per_s": stats_bytes / (stats_ms * 1e-3) / 1e9},
+        "also": also,
+    }
+    if rank == 0 and not a.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_rate(w, a.cpu_rows, os.cpu_count() or 1)
+    return line
+
+
+def run_reference(a, rank, world):
+    """The float64 CPU oracle as the reference arm: same workload and metric, bounded rows per step."""
+    if rank != 0:
+        return None
+    k = int(a.workload.lstrip("c"))
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    w = W.make(k, device=dev)
+    procs = os.cpu_count() or 1
+    rates = []
+    with oracle_pool(procs) as pool:
+        for _ in range(a.warmup):
+            cpu_oracle_rate(w, min(a.ref_rows, procs), procs, pool)
+        t0 = time.perf_counter()
+        for _ in range(a.steps):
+            rates.append(cpu_oracle_rate(w, a.ref_rows, procs, pool)["value"])
+            if time.perf_counter() - t0 > 180:      # bounded: the whole run stays within a few minutes
+                break
+    v = statistics.median(rates)
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": len(rates),
+            "warmup": a.warmup, "ms_per_step": w.positions() / v * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded Philox workload, see workloads/)",
+            "config": workload_desc(w),
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": procs, "kind": "oracle",
+                             "sample": f"{a.ref_rows} rows of {w.name} per step, median of {len(rates)} steps"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="c3", choices=["c1", "c2", "c3", "c4"])
+    ap.add_argument("--cpu-rows", type=int, default=512)
+    ap.add_argument("--ref-rows", type=int, default=64)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-also", action="store_true")
+    a = ap.parse_args()
+    a.warmup = max(3, a.warmup)
+
+    rank, world, dist = dist_init()
+    if a.impl == "reference":
+        line = run_reference(a, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU for --impl ours")
+    import __graft_entry__
+    __graft_entry__.build()
+    line = run_ours(a, rank, world, dist)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,150 @@
+/*
+ * spec_verify.h -- C ABI of the batched verification step of speculative
+ * sampling, for one NVIDIA GB300 (sm_103a).
+ *
+ * The method is Algorithm 1 of Leviathan, Kalman & Matias, "Fast Inference
+ * from Transformers via Speculative Decoding" (arXiv 2211.17192), as restated
+ * in the paper-graph-ui teardown of that paper (§2.2 "Standardized Sampling",
+ * §2.3 "Algorithm Walkthrough", Phases 3-4), the multigrid.ai explainer
+ * "Speculative Decoding: Two Models, One Output" ("The algorithm"), the
+ * fullstackaihub "Speculative Decoding Paper Breakdown" (§3 "The Algorithm at
+ * Position i") and the interactiveml post on the correction distribution.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer argument except `workspace` of spec_workspace_size is a
+ *    DEVICE pointer (cudaMalloc / torch CUDA memory) of the current device.
+ *    The caller owns all buffers; the library allocates nothing and keeps no
+ *    state between calls except what it leaves in the caller's workspace.
+ *  - All arrays are dense row-major.  Logits are IEEE float32 (SPEC_F32) or
+ *    bfloat16 (SPEC_BF16); the target holds gamma+1 rows of V per batch row b,
+ *    the draft gamma rows of V.  gamma is the padded draft width.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Calls are asynchronous on it.  The return value covers host-side
+ *    argument checks and launch errors only.  What the device finds
+ *    (non-finite logit rows, draft ids outside [0, V), uniforms outside
+ *    [0, 1), draft_len outside [0, gamma]) marks the affected batch row
+ *    invalid -- n_accepted[b] = -1 and emitted[b, :] = -1 -- and is recorded in
+ *    the workspace's error word, read by spec_check_status.
+ *  - A row is invalid if any logit row it reads holds a NaN or +inf or is
+ *    entirely -inf.  Ragged rows (draft_len[b] = gamma_b < gamma) never read
+ *    target rows i > gamma_b, draft rows i >= gamma_b, ids i >= gamma_b, or
+ *    uniforms gamma_b <= i < gamma.
+ *  - Limits: B >= 0 (B = 0 is a no-op), 0 <= gamma <= SPEC_MAX_GAMMA,
+ *    1 <= V <= SPEC_MAX_VOCAB.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SPEC_MAX_GAMMA 64
+#define SPEC_MAX_VOCAB 262144
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype_t;
+
+typedef enum {
+  SPEC_OK = 0,
+  SPEC_ERR_ARG = 1,          /* bad size, null pointer, temperature, draft_len or uniform */
+  SPEC_ERR_DTYPE = 2,        /* unknown dtype */
+  SPEC_ERR_CUDA = 3,         /* a CUDA runtime call failed */
+  SPEC_ERR_NONFINITE = 4,    /* a logit row read holds NaN / +inf or is all -inf */
+  SPEC_ERR_TOKEN_RANGE = 5,  /* a draft id read lies outside [0, V) */
+  SPEC_ERR_TIMEOUT = 6,      /* reserved: no entry point waits on another block */
+  SPEC_ERR_WORKSPACE = 7     /* workspace too small or not 256-byte aligned */
+} spec_status_t;
+
+/* Bytes of device workspace the three entry points need for (B, gamma): an
+ * error word, a per-row arrival counter and per-position records.  The
+ * workspace must be zero-filled once before its first use (cudaMemset or
+ * spec_workspace_init); every call leaves the counters and records it used at
+ * zero again, so one workspace serves any sequence of calls on one stream.
+ * Calls that overlap on the GPU must use different workspaces.  Returns 0 for
+ * invalid sizes.  No CUDA call is made. */
+size_t spec_workspace_size(int B, int gamma, int V, int dtype);
+
+/* Zero-fills `ws_bytes` of workspace on `stream` (cudaMemsetAsync). */
+int spec_workspace_init(void* workspace, size_t ws_bytes, void* stream);
+
+/* Speculative sampling verification, Algorithm 1 Phases 3-4 (paper-graph-ui
+ * teardown §2.3; multigrid.ai "The algorithm"; fullstackaihub §3).
+ *
+ * For each batch row b with gamma_b = draft_len[b] (or gamma if draft_len is
+ * NULL):  p_i = softmax(target[b,i,:] / T) for i <= gamma_b and q_i =
+ * softmax(draft[b,i,:] / T) for i < gamma_b (temperature standardisation,
+ * §2.2).  Guess x_i = draft_ids[b,i] is accepted iff p_i(x_i) > 0 and
+ * uniforms[b,i] <= min(1, p_i(x_i)/q_i(x_i)); the walk stops at the first
+ * rejection, n = n_accepted[b].  If n < gamma_b the emitted token is drawn from
+ * norm(max(0, p_n - q_n)) (from p_n if that residual mass is <= 1e-15, the
+ * interactiveml correction rule), else from p_{gamma_b} (bonus token).  The
+ * draw is an inverse CDF driven by uniforms[b, gamma]: the smallest token k
+ * whose running weight sum exceeds uniforms[b,gamma] * (total weight).
+ *
+ *   target_logits  [B, gamma+1, V]  dtype
+ *   draft_logits   [B, gamma, V]    dtype (may be NULL when gamma == 0)
+ *   draft_ids      [B, gamma]       int32 (may be NULL when gamma == 0)
+ *   draft_len      [B]              int32 in [0, gamma], or NULL for all gamma
+ *   uniforms       [B, gamma+1]     float32 in [0, 1)
+ *   temperature    > 0, finite
+ *   emitted        [B, gamma+1]     int32 out: x_0..x_{n-1}, the drawn token, then -1
+ *   n_accepted     [B]              int32 out: n in [0, gamma_b], or -1 for an invalid row
+ *   workspace      >= spec_workspace_size(B, gamma, V, dtype) bytes, 256-byte aligned
+ */
+int spec_verify_sample(const void* target_logits, const void* draft_logits, int dtype,
+                       const int32_t* draft_ids, const int32_t* draft_len, const float* uniforms,
+                       float temperature, int B, int gamma, int V,
+                       int32_t* emitted, int32_t* n_accepted,
+                       void* workspace, size_t ws_bytes, void* stream);
+
+/* Greedy verification: argmax standardisation (paper-graph-ui teardown §2.2;
+ * multigrid.ai on sampling temperature).  a_i = argmax_k target[b,i,k], lowest
+ * index on ties; guesses are accepted while a_i == draft_ids[b,i]; the emitted
+ * token at n is a_n (n < gamma_b) or a_{gamma_b}.  Reads the target logits
+ * only; draft_logits is accepted for symmetry and never read (may be NULL).
+ * Outputs and errors as spec_verify_sample. */
+int spec_verify_greedy(const void* target_logits, const void* draft_logits, int dtype,
+                       const int32_t* draft_ids, const int32_t* draft_len,
+                       int B, int gamma, int V,
+                       int32_t* emitted, int32_t* n_accepted,
+                       void* workspace, size_t ws_bytes, void* stream);
+
+/* Per-position acceptance statistics (paper-graph-ui teardown Definition 3.2,
+ * Lemma 3.3, Theorem 3.5): for i < gamma_b,
+ *   beta[b,i]        = sum_x min(p_i(x), q_i(x))     (acceptance rate, 1 - DLK)
+ *   p_draft[b,i]     = p_i(x_i),  q_draft[b,i] = q_i(x_i)
+ *   accept_prob[b,i] = min(1, p_i(x_i)/q_i(x_i)), 0 if p_i(x_i) = 0
+ *   resid_mass[b,i]  = sum_x max(0, p_i(x) - q_i(x))  (residual normaliser)
+ * Each output is [B, gamma] float32 and may be NULL.  Positions i >= gamma_b
+ * and invalid positions get NaN. */
+int spec_accept_stats(const void* target_logits, const void* draft_logits, int dtype,
+                      const int32_t* draft_ids, const int32_t* draft_len, float temperature,
+                      int B, int gamma, int V,
+                      float* beta, float* p_draft, float* q_draft, float* accept_prob,
+                      float* resid_mass,
+                      void* workspace, size_t ws_bytes, void* stream);
+
+/* Synchronises `stream`, reads and clears the workspace's error word, and
+ * returns the lowest-numbered spec_status_t it records (SPEC_OK if none). */
+int spec_check_status(void* workspace, void* stream);
+
+/* Launch plan the sampling / statistics kernel would use for (B, gamma, V,
+ * dtype) on the current device: thread-block cluster size (CTAs per
+ * vocabulary row), slice length per CTA, dynamic shared memory per CTA, CTAs
+ * per row for the greedy kernel.  Any output pointer may be NULL.  Host
+ * pointers. */
+int spec_verify_plan(int B, int gamma, int V, int dtype, int* cluster_size, int* slice_len,
+                     int* smem_bytes, int* greedy_ctas_per_row);
+
+/* Static text for a spec_status_t. */
+const char* spec_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

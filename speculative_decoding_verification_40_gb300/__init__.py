@@ -1,0 +1,231 @@
+"""Batched speculative-sampling verification on one GB300 (sm_103a).
+
+Python binding of libspecverify.so, the C-ABI library declared in
+include/spec_verify.h.  The functions here only marshal torch CUDA tensors
+(device pointers, sizes, the current stream) into the C calls: every step of
+the verification runs in the library's CUDA kernels.  Importing this package
+fails if the library has not been built
+(python -m speculative_decoding_verification_40_gb300.build).
+
+Entry points (same names as the C ABI, without the spec_ prefix):
+  verify_sample  -- accept test, first rejection, residual / bonus draw
+  verify_greedy  -- argmax verification
+  accept_stats   -- per-position beta, p(x), q(x), min(1, p/q), residual mass
+  check_status   -- device-side error word of a workspace
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "SpecVerifyError", "verify_sample", "verify_greedy", "accept_stats", "check_status", "workspace_size",
+    "workspace_for", "plan", "LIB_PATH", "lib",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libspecverify.so")
+
+SPEC_F32, SPEC_BF16 = 0, 1
+STATUS = {0: "ok", 1: "invalid argument", 2: "unknown dtype", 3: "CUDA error", 4: "non-finite or all -inf logit row",
+          5: "draft id outside [0, V)", 6: "timeout", 7: "workspace too small or misaligned"}
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS.get(code, 'unknown status')} (code {code})")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with "
+                          "`python -m speculative_decoding_verification_40_gb300.build`")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.spec_workspace_size.argtypes = [i32, i32, i32, i32]
+    L.spec_workspace_size.restype = sz
+    L.spec_workspace_init.argtypes = [vp, sz, vp]
+    L.spec_workspace_init.restype = i32
+    L.spec_verify_sample.argtypes = [vp, vp, i32, vp, vp, vp, f32, i32, i32, i32, vp, vp, vp, sz, vp]
+    L.spec_verify_sample.restype = i32
+    L.spec_verify_greedy.argtypes = [vp, vp, i32, vp, vp, i32, i32, i32, vp, vp, vp, sz, vp]
+    L.spec_verify_greedy.restype = i32
+    L.spec_accept_stats.argtypes = [vp, vp, i32, vp, vp, f32, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.spec_accept_stats.restype = i32
+    L.spec_check_status.argtypes = [vp, vp]
+    L.spec_check_status.restype = i32
+    ip = ctypes.POINTER(ctypes.c_int)
+    L.spec_verify_plan.argtypes = [i32, i32, i32, i32, ip, ip, ip, ip]
+    L.spec_verify_plan.restype = i32
+    L.spec_status_string.argtypes = [i32]
+    L.spec_status_string.restype = ctypes.c_char_p
+    return L
+
+
+lib = _load()
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SPEC_F32
+    if t.dtype == torch.bfloat16:
+        return SPEC_BF16
+    raise TypeError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def _p(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _cuda(t: torch.Tensor, name: str, dtype=None, shape=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t
+
+
+def _stream(device: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _raise(code: int, where: str):
+    if code != 0:
+        raise SpecVerifyError(code, where)
+
+
+def workspace_size(B: int, gamma: int, V: int, dtype: torch.dtype = torch.float32) -> int:
+    code = SPEC_BF16 if dtype == torch.bfloat16 else SPEC_F32
+    return int(lib.spec_workspace_size(B, gamma, V, code))
+
+
+_WS: dict = {}
+
+
+def workspace_for(device: torch.device, nbytes: int) -> torch.Tensor:
+    """Zero-filled per-device workspace of at least nbytes, grown on demand.
+
+    The library leaves every counter it uses at zero after each call, so one
+    workspace serves any sequence of calls on one stream; calls that may
+    overlap on the GPU need workspaces of their own (pass `workspace=`).
+    """
+    device = torch.device(device)
+    key = (device.type, device.index if device.index is not None else torch.cuda.current_device())
+    ws = _WS.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(nbytes, 4096), dtype=torch.uint8, device=device)
+        _WS[key] = ws
+    return ws
+
+
+def plan(B: int, gamma: int, V: int, dtype: torch.dtype = torch.float32) -> dict:
+    """Launch plan of the sampling kernel: cluster size, slice length, shared memory, greedy CTAs per row."""
+    cs, L, sm, g = (ctypes.c_int() for _ in range(4))
+    code = SPEC_BF16 if dtype == torch.bfloat16 else SPEC_F32
+    _raise(lib.spec_verify_plan(B, gamma, V, code, ctypes.byref(cs), ctypes.byref(L), ctypes.byref(sm),
+                                ctypes.byref(g)), "spec_verify_plan")
+    return {"cluster_size": cs.value, "slice_len": L.value, "smem_bytes": sm.value, "greedy_ctas_per_row": g.value}
+
+
+def check_status(workspace: torch.Tensor | None = None, device=None, raise_on_error: bool = True) -> int:
+    """Synchronise the current stream, read and clear the workspace's device error word."""
+    if workspace is None:
+        device = torch.device(device or "cuda")
+        workspace = workspace_for(device, 4096)
+    code = int(lib.spec_check_status(_p(workspace), _stream(workspace.device)))
+    if raise_on_error:
+        _raise(code, "device")
+    return code
+
+
+def _shapes(target: torch.Tensor):
+    if target.dim() != 3:
+        raise ValueError("target logits must be [B, gamma+1, V]")
+    B, G1, V = target.shape
+    return B, G1 - 1, V
+
+
+def _common(target, draft, ids, draft_len, gamma_needs_draft=True):
+    B, G, V = _shapes(target)
+    _cuda(target, "target_logits")
+    if G > 0 and gamma_needs_draft:
+        _cuda(draft, "draft_logits", target.dtype, (B, G, V))
+    if G > 0:
+        _cuda(ids, "draft_ids", torch.int32, (B, G))
+    if draft_len is not None:
+        _cuda(draft_len, "draft_len", torch.int32, (B,))
+    return B, G, V
+
+
+# ----------------------------------------------------------------------------- entry points
+
+def verify_sample(target: torch.Tensor, draft: torch.Tensor, ids: torch.Tensor, uniforms: torch.Tensor,
+                  temperature: float, draft_len: torch.Tensor | None = None, *, emitted=None, n_accepted=None,
+                  workspace: torch.Tensor | None = None, check: bool = False):
+    """spec_verify_sample: returns (emitted [B, gamma+1] int32, n_accepted [B] int32)."""
+    B, G, V = _common(target, draft, ids, draft_len)
+    _cuda(uniforms, "uniforms", torch.float32, (B, G + 1))
+    dev = target.device
+    if emitted is None:
+        emitted = torch.empty(B, G + 1, dtype=torch.int32, device=dev)
+    if n_accepted is None:
+        n_accepted = torch.empty(B, dtype=torch.int32, device=dev)
+    _cuda(emitted, "emitted", torch.int32, (B, G + 1))
+    _cuda(n_accepted, "n_accepted", torch.int32, (B,))
+    ws = workspace if workspace is not None else workspace_for(dev, workspace_size(B, G, V, target.dtype))
+    code = lib.spec_verify_sample(_p(target), _p(draft) if G > 0 else None, _dtype_code(target),
+                                  _p(ids) if G > 0 else None, _p(draft_len), _p(uniforms), float(temperature),
+                                  B, G, V, _p(emitted), _p(n_accepted), _p(ws), ws.numel(), _stream(dev))
+    _raise(code, "spec_verify_sample")
+    if check:
+        check_status(ws)
+    return emitted, n_accepted
+
+
+def verify_greedy(target: torch.Tensor, ids: torch.Tensor, draft_len: torch.Tensor | None = None,
+                  draft: torch.Tensor | None = None, *, emitted=None, n_accepted=None,
+                  workspace: torch.Tensor | None = None, check: bool = False):
+    """spec_verify_greedy: returns (emitted [B, gamma+1] int32, n_accepted [B] int32)."""
+    B, G, V = _common(target, draft, ids, draft_len, gamma_needs_draft=False)
+    dev = target.device
+    if emitted is None:
+        emitted = torch.empty(B, G + 1, dtype=torch.int32, device=dev)
+    if n_accepted is None:
+        n_accepted = torch.empty(B, dtype=torch.int32, device=dev)
+    _cuda(emitted, "emitted", torch.int32, (B, G + 1))
+    _cuda(n_accepted, "n_accepted", torch.int32, (B,))
+    ws = workspace if workspace is not None else workspace_for(dev, workspace_size(B, G, V, target.dtype))
+    code = lib.spec_verify_greedy(_p(target), _p(draft), _dtype_code(target), _p(ids) if G > 0 else None,
+                                  _p(draft_len), B, G, V, _p(emitted), _p(n_accepted), _p(ws), ws.numel(),
+                                  _stream(dev))
+    _raise(code, "spec_verify_greedy")
+    if check:
+        check_status(ws)
+    return emitted, n_accepted
+
+
+def accept_stats(target: torch.Tensor, draft: torch.Tensor, ids: torch.Tensor, temperature: float,
+                 draft_len: torch.Tensor | None = None, *, workspace: torch.Tensor | None = None,
+                 check: bool = False) -> dict:
+    """spec_accept_stats: dict of [B, gamma] float32 tensors beta, p_x, q_x, accept_prob, resid."""
+    B, G, V = _common(target, draft, ids, draft_len)
+    dev = target.device
+    out = {k: torch.empty(B, G, dtype=torch.float32, device=dev) for k in ("beta", "p_x", "q_x", "accept_prob",
+                                                                          "resid")}
+    ws = workspace if workspace is not None else workspace_for(dev, workspace_size(B, G, V, target.dtype))
+    code = lib.spec_accept_stats(_p(target), _p(draft) if G > 0 else None, _dtype_code(target),
+                                 _p(ids) if G > 0 else None, _p(draft_len), float(temperature), B, G, V,
+                                 _p(out["beta"]), _p(out["p_x"]), _p(out["q_x"]), _p(out["accept_prob"]),
+                                 _p(out["resid"]), _p(ws), ws.numel(), _stream(dev))
+    _raise(code, "spec_accept_stats")
+    if check:
+        check_status(ws)
+    return out

@@ -1,0 +1,321 @@
+// C ABI of the verification library: argument checks, launch plan, launches.
+// The operations are specified in include/spec_verify.h.
+#include <atomic>
+#include <cmath>
+#include <cstdlib>
+#include <mutex>
+#include <vector>
+
+#include "../../include/spec_verify.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace {
+
+using specv::align_up;
+
+constexpr int kSmemPreferred = 100 * 1024;  // leaves room for two CTAs per SM
+constexpr int kSmemMax = 227 * 1024 - 2048; // opt-in limit minus the kernel's static shared memory
+constexpr int kMaxDevices = 64;
+
+struct Plan {
+  int cs;     // CTAs per cluster (vocabulary slices per row)
+  int L;      // slice length in elements
+  int smem;   // dynamic shared memory per CTA
+};
+
+int smem_for(int L) {
+  const int Lpad = static_cast<int>(align_up(L, specv::kChunk));
+  return 2 * Lpad * 4 + 2 * (Lpad / specv::kChunk) * 4;
+}
+
+Plan plan_for(int V, int cs) {
+  Plan p;
+  p.cs = cs;
+  p.L = static_cast<int>(align_up((V + cs - 1) / cs, 8));
+  p.smem = smem_for(p.L);
+  return p;
+}
+
+// Smallest cluster whose slice fits the preferred shared-memory budget; an
+// explicit SPECVERIFY_CLUSTER (1, 2, 4, 8 or 16) overrides the choice.
+bool choose_plan(int V, Plan* out) {
+  if (const char* env = std::getenv("SPECVERIFY_CLUSTER")) {
+    const int cs = std::atoi(env);
+    if (cs == 1 || cs == 2 || cs == 4 || cs == 8 || cs == 16) {
+      Plan p = plan_for(V, cs);
+      if (p.smem <= kSmemMax) {
+        *out = p;
+        return true;
+      }
+    }
+  }
+  for (int cs = 1; cs <= specv::kMaxCluster; cs *= 2) {
+    Plan p = plan_for(V, cs);
+    if (p.smem <= kSmemPreferred) {
+      *out = p;
+      return true;
+    }
+  }
+  for (int cs = 1; cs <= specv::kMaxCluster; cs *= 2) {
+    Plan p = plan_for(V, cs);
+    if (p.smem <= kSmemMax) {
+      *out = p;
+      return true;
+    }
+  }
+  return false;
+}
+
+// Kernel attributes are per device; set them once per (device, kernel, dtype).
+std::atomic<int> g_prepared[kMaxDevices][2][2];
+std::mutex g_prep_mu;
+
+int prepare(int dtype, bool stats) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPEC_ERR_CUDA;
+  std::atomic<int>& flag = g_prepared[dev][dtype][stats ? 1 : 0];
+  if (flag.load(std::memory_order_acquire)) return SPEC_OK;
+  std::lock_guard<std::mutex> lk(g_prep_mu);
+  if (!flag.load(std::memory_order_relaxed)) {
+    if (specv::verify_prepare(dtype, stats, kSmemMax) != cudaSuccess) return SPEC_ERR_CUDA;
+    flag.store(1, std::memory_order_release);
+  }
+  return SPEC_OK;
+}
+
+// Falls back to smaller clusters when the device cannot co-schedule the planned one.
+int schedulable_plan(int V, int dtype, bool stats, Plan* plan) {
+  for (int tries = 0; tries < 5; ++tries) {
+    int n = 0;
+    if (specv::verify_max_active_clusters(dtype, stats, plan->cs, plan->smem, &n) != cudaSuccess) {
+      cudaGetLastError();
+      return SPEC_ERR_CUDA;
+    }
+    if (n > 0) return SPEC_OK;
+    if (plan->cs == 1) return SPEC_ERR_ARG;
+    Plan q = plan_for(V, plan->cs / 2);
+    if (q.smem > kSmemMax) return SPEC_ERR_ARG;
+    *plan = q;
+  }
+  return SPEC_ERR_ARG;
+}
+
+// Plans already resolved on a device (the occupancy query costs tens of microseconds).
+struct PlanEntry {
+  int dev, V, dtype, stats, env_cs;
+  Plan plan;
+};
+std::mutex g_plan_mu;
+std::vector<PlanEntry> g_plans;
+
+int env_cluster() {
+  const char* env = std::getenv("SPECVERIFY_CLUSTER");
+  return env ? std::atoi(env) : 0;
+}
+
+int resolve_plan(int V, int dtype, bool stats, Plan* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return SPEC_ERR_CUDA;
+  }
+  const int env_cs = env_cluster();
+  {
+    std::lock_guard<std::mutex> lk(g_plan_mu);
+    for (const PlanEntry& e : g_plans) {
+      if (e.dev == dev && e.V == V && e.dtype == dtype && e.stats == (stats ? 1 : 0) && e.env_cs == env_cs) {
+        *out = e.plan;
+        return SPEC_OK;
+      }
+    }
+  }
+  Plan plan;
+  if (!choose_plan(V, &plan)) return SPEC_ERR_ARG;
+  int st = prepare(dtype, stats);
+  if (st != SPEC_OK) return st;
+  if ((st = schedulable_plan(V, dtype, stats, &plan)) != SPEC_OK) return st;
+  std::lock_guard<std::mutex> lk(g_plan_mu);
+  if (g_plans.size() < 4096) g_plans.push_back(PlanEntry{dev, V, dtype, stats ? 1 : 0, env_cs, plan});
+  *out = plan;
+  return SPEC_OK;
+}
+
+bool rows_aligned(const void* p, int V, int esz) {
+  return (reinterpret_cast<uintptr_t>(p) % 16 == 0) && ((static_cast<size_t>(V) * esz) % 16 == 0);
+}
+
+int check_sizes(int dtype, int B, int gamma, int V) {
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
+  if (B < 0 || gamma < 0 || gamma > SPEC_MAX_GAMMA || V < 1 || V > SPEC_MAX_VOCAB) return SPEC_ERR_ARG;
+  // grid size: B * (gamma+1) * max(cluster size, greedy CTAs per row) CTAs
+  const long long per_row = SPEC_MAX_VOCAB / specv::kGreedySlice;
+  if ((long long)B * (gamma + 1) * per_row > 0x7fffffffLL) return SPEC_ERR_ARG;
+  return SPEC_OK;
+}
+
+int check_common(int dtype, int B, int gamma, int V, const void* workspace, size_t ws_bytes) {
+  const int st = check_sizes(dtype, B, gamma, V);
+  if (st != SPEC_OK || B == 0) return st;
+  if (workspace == nullptr || reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return SPEC_ERR_WORKSPACE;
+  if (ws_bytes < specv::ws_bytes_for(B, gamma)) return SPEC_ERR_WORKSPACE;
+  return SPEC_OK;
+}
+
+int launch_status(cudaError_t e) {
+  if (e == cudaSuccess) return SPEC_OK;
+  cudaGetLastError();
+  return SPEC_ERR_CUDA;
+}
+
+int run_verify(const void* target, const void* draft, int dtype, const int32_t* ids, const int32_t* draft_len,
+               const float* uniforms, float temperature, int B, int gamma, int V, int32_t* emitted,
+               int32_t* n_accepted, float* beta, float* p_draft, float* q_draft, float* accept_prob,
+               float* resid, void* workspace, size_t ws_bytes, void* stream, bool stats) {
+  int st = check_common(dtype, B, gamma, V, workspace, ws_bytes);
+  if (st != SPEC_OK) return st;
+  if (!(std::isfinite(temperature) && temperature > 0.f)) return SPEC_ERR_ARG;
+  if (B == 0 || (stats && gamma == 0)) return SPEC_OK;
+  if (target == nullptr) return SPEC_ERR_ARG;
+  if (gamma > 0 && (draft == nullptr || ids == nullptr)) return SPEC_ERR_ARG;
+  if (!stats && (uniforms == nullptr || emitted == nullptr || n_accepted == nullptr)) return SPEC_ERR_ARG;
+
+  Plan plan;
+  if ((st = resolve_plan(V, dtype, stats, &plan)) != SPEC_OK) return st;
+
+  const int esz = dtype == SPEC_F32 ? 4 : 2;
+  specv::VerifyParams p = {};
+  p.target = target;
+  p.draft = draft;
+  p.ids = ids;
+  p.draft_len = draft_len;
+  p.uniforms = uniforms;
+  p.scale = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+  p.B = B;
+  p.G = gamma;
+  p.V = V;
+  p.L = plan.L;
+  p.vec = rows_aligned(target, V, esz) && (gamma == 0 || rows_aligned(draft, V, esz)) ? 1 : 0;
+  p.emitted = emitted;
+  p.n_acc = n_accepted;
+  p.beta = beta;
+  p.p_draft = p_draft;
+  p.q_draft = q_draft;
+  p.accept_prob = accept_prob;
+  p.resid = resid;
+  p.ws = specv::ws_carve(workspace, B, gamma);
+  return launch_status(
+      specv::verify_launch(p, dtype, stats, plan.cs, plan.smem, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t spec_workspace_size(int B, int gamma, int V, int dtype) {
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return 0;
+  if (B < 0 || gamma < 0 || gamma > SPEC_MAX_GAMMA || V < 1 || V > SPEC_MAX_VOCAB) return 0;
+  return specv::ws_bytes_for(B, gamma);
+}
+
+int spec_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
+  if (workspace == nullptr) return SPEC_ERR_WORKSPACE;
+  return launch_status(cudaMemsetAsync(workspace, 0, ws_bytes, static_cast<cudaStream_t>(stream)));
+}
+
+int spec_verify_sample(const void* target_logits, const void* draft_logits, int dtype, const int32_t* draft_ids,
+                       const int32_t* draft_len, const float* uniforms, float temperature, int B, int gamma, int V,
+                       int32_t* emitted, int32_t* n_accepted, void* workspace, size_t ws_bytes, void* stream) {
+  return run_verify(target_logits, draft_logits, dtype, draft_ids, draft_len, uniforms, temperature, B, gamma, V,
+                    emitted, n_accepted, nullptr, nullptr, nullptr, nullptr, nullptr, workspace, ws_bytes, stream,
+                    false);
+}
+
+int spec_accept_stats(const void* target_logits, const void* draft_logits, int dtype, const int32_t* draft_ids,
+                      const int32_t* draft_len, float temperature, int B, int gamma, int V, float* beta,
+                      float* p_draft, float* q_draft, float* accept_prob, float* resid_mass, void* workspace,
+                      size_t ws_bytes, void* stream) {
+  return run_verify(target_logits, draft_logits, dtype, draft_ids, draft_len, nullptr, temperature, B, gamma, V,
+                    nullptr, nullptr, beta, p_draft, q_draft, accept_prob, resid_mass, workspace, ws_bytes, stream,
+                    true);
+}
+
+int spec_verify_greedy(const void* target_logits, const void* draft_logits, int dtype, const int32_t* draft_ids,
+                       const int32_t* draft_len, int B, int gamma, int V, int32_t* emitted, int32_t* n_accepted,
+                       void* workspace, size_t ws_bytes, void* stream) {
+  (void)draft_logits;
+  int st = check_common(dtype, B, gamma, V, workspace, ws_bytes);
+  if (st != SPEC_OK) return st;
+  if (B == 0) return SPEC_OK;
+  if (target_logits == nullptr || emitted == nullptr || n_accepted == nullptr) return SPEC_ERR_ARG;
+  if (gamma > 0 && draft_ids == nullptr) return SPEC_ERR_ARG;
+  const int esz = dtype == SPEC_F32 ? 4 : 2;
+  specv::GreedyParams p = {};
+  p.target = target_logits;
+  p.ids = draft_ids;
+  p.draft_len = draft_len;
+  p.B = B;
+  p.G = gamma;
+  p.V = V;
+  p.slice = specv::kGreedySlice;
+  p.nslices = (V + p.slice - 1) / p.slice;
+  p.vec = rows_aligned(target_logits, V, esz) ? 1 : 0;
+  p.emitted = emitted;
+  p.n_acc = n_accepted;
+  p.ws = specv::ws_carve(workspace, B, gamma);
+  return launch_status(specv::greedy_launch(p, dtype, static_cast<cudaStream_t>(stream)));
+}
+
+int spec_check_status(void* workspace, void* stream) {
+  if (workspace == nullptr) return SPEC_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return SPEC_ERR_CUDA;
+  }
+  if (word == 0) return SPEC_OK;
+  if (cudaMemsetAsync(workspace, 0, sizeof(word), s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return SPEC_ERR_CUDA;
+  }
+  for (int code = 1; code < 32; ++code)
+    if (word & (1u << code)) return code;
+  return SPEC_ERR_CUDA;
+}
+
+int spec_verify_plan(int B, int gamma, int V, int dtype, int* cluster_size, int* slice_len, int* smem_bytes,
+                     int* greedy_ctas_per_row) {
+  int st = check_sizes(dtype, B, gamma, V);
+  if (st != SPEC_OK) return st;
+  Plan plan;
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    if ((st = resolve_plan(V, dtype, false, &plan)) != SPEC_OK) return st;
+  } else {
+    cudaGetLastError();  // no device: report the plan before the co-scheduling check
+    if (!choose_plan(V, &plan)) return SPEC_ERR_ARG;
+  }
+  if (cluster_size) *cluster_size = plan.cs;
+  if (slice_len) *slice_len = plan.L;
+  if (smem_bytes) *smem_bytes = plan.smem;
+  if (greedy_ctas_per_row) *greedy_ctas_per_row = (V + specv::kGreedySlice - 1) / specv::kGreedySlice;
+  return SPEC_OK;
+}
+
+const char* spec_status_string(int status) {
+  switch (status) {
+    case SPEC_OK: return "ok";
+    case SPEC_ERR_ARG: return "invalid argument";
+    case SPEC_ERR_DTYPE: return "unknown dtype";
+    case SPEC_ERR_CUDA: return "CUDA error";
+    case SPEC_ERR_NONFINITE: return "non-finite or all -inf logit row";
+    case SPEC_ERR_TOKEN_RANGE: return "draft id outside [0, V)";
+    case SPEC_ERR_TIMEOUT: return "timeout";
+    case SPEC_ERR_WORKSPACE: return "workspace too small or misaligned";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

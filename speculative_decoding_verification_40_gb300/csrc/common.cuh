@@ -1,0 +1,175 @@
+// Device-side building blocks shared by the verification kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace specv {
+
+// ---------------------------------------------------------------- launch constants
+constexpr int kThreads = 512;          // threads per CTA of the sampling / statistics kernel
+constexpr int kWarps = kThreads / 32;
+constexpr int kChunk = 128;            // elements per warp-chunk: 32 lanes x 4 consecutive elements
+constexpr int kMaxCluster = 16;        // largest thread-block cluster (non-portable size)
+constexpr int kGreedyThreads = 256;    // threads per CTA of the greedy kernel
+constexpr int kGreedySlice = 8192;     // target-row elements per greedy CTA
+
+// Device error word: bit k is set for spec_status_t k.
+constexpr uint32_t kErrArg = 1u << 1;
+constexpr uint32_t kErrNonfinite = 1u << 4;
+constexpr uint32_t kErrToken = 1u << 5;
+
+// Residual-mass floor below which the draw falls back to p (interactiveml correction rule).
+constexpr float kZFloor = 1e-15f;
+
+// ---------------------------------------------------------------- workspace
+struct Workspace {
+  uint32_t* err;             // error word (bits above)
+  uint32_t* ticket;          // [B] arrivals of position clusters / slice CTAs per batch row
+  int32_t* acc;              // [B, G+1] per position: 1 accept, 0 reject, -1 invalid
+  int32_t* tok;              // [B, G+1] token drawn if the walk stops at this position
+  unsigned long long* key;   // [B, G+1] greedy (value, index) argmax keys
+};
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+__host__ __device__ inline size_t ws_bytes_for(int B, int G) {
+  const size_t P = (size_t)B * (size_t)(G + 1);
+  return 256 + align_up((size_t)B * 4, 256) + 2 * align_up(P * 4, 256) + align_up(P * 8, 256);
+}
+
+inline Workspace ws_carve(void* base, int B, int G) {
+  const size_t P = (size_t)B * (size_t)(G + 1);
+  char* p = static_cast<char*>(base);
+  Workspace w;
+  w.err = reinterpret_cast<uint32_t*>(p);
+  p += 256;
+  w.ticket = reinterpret_cast<uint32_t*>(p);
+  p += align_up((size_t)B * 4, 256);
+  w.acc = reinterpret_cast<int32_t*>(p);
+  p += align_up(P * 4, 256);
+  w.tok = reinterpret_cast<int32_t*>(p);
+  p += align_up(P * 4, 256);
+  w.key = reinterpret_cast<unsigned long long*>(p);
+  return w;
+}
+
+#ifdef __CUDACC__
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+
+// Cluster-wide barrier; release/acquire orders shared-memory writes before it
+// with distributed-shared-memory reads after it.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Address of the same shared-memory variable in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t dsmem_map(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ float dsmem_ld_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// 16-byte streaming load of read-only data: no L1 allocation.
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+
+// max that propagates NaN: a NaN anywhere in a row survives the reduction.
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max_nan(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max_nan(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Inclusive prefix sum across the warp's lanes.
+__device__ __forceinline__ float warp_inclusive_scan(float v, int lane) {
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, v, d);
+    if (lane >= d) v += y;
+  }
+  return v;
+}
+// ---------------------------------------------------------------- logit element access
+template <typename T>
+struct Elems;
+
+template <>
+struct Elems<float> {
+  static constexpr int kVec = 4;  // elements per 16-byte load
+  __device__ static __forceinline__ void widen(const uint4& r, float* f) {
+    f[0] = __uint_as_float(r.x);
+    f[1] = __uint_as_float(r.y);
+    f[2] = __uint_as_float(r.z);
+    f[3] = __uint_as_float(r.w);
+  }
+  __device__ static __forceinline__ float one(const float* p, int k) { return __ldg(p + k); }
+};
+
+template <>
+struct Elems<__nv_bfloat16> {
+  static constexpr int kVec = 8;
+  __device__ static __forceinline__ void widen(const uint4& r, float* f) {
+    f[0] = __uint_as_float(r.x << 16);
+    f[1] = __uint_as_float(r.x & 0xffff0000u);
+    f[2] = __uint_as_float(r.y << 16);
+    f[3] = __uint_as_float(r.y & 0xffff0000u);
+    f[4] = __uint_as_float(r.z << 16);
+    f[5] = __uint_as_float(r.z & 0xffff0000u);
+    f[6] = __uint_as_float(r.w << 16);
+    f[7] = __uint_as_float(r.w & 0xffff0000u);
+  }
+  __device__ static __forceinline__ float one(const __nv_bfloat16* p, int k) {
+    const unsigned short bits = __ldg(reinterpret_cast<const unsigned short*>(p) + k);
+    return __uint_as_float(static_cast<uint32_t>(bits) << 16);
+  }
+};
+
+template <int kVec>
+__device__ __forceinline__ void store_f32(float* dst, const float* f) {
+#pragma unroll
+  for (int j = 0; j < kVec; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]);
+}
+
+#endif  // __CUDACC__
+
+}  // namespace specv

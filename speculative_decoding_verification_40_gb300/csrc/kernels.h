@@ -1,0 +1,50 @@
+// Parameters and host launchers of the verification kernels (internal to the library).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace specv {
+
+struct VerifyParams {
+  const void* target;        // [B, G+1, V]
+  const void* draft;         // [B, G, V]
+  const int32_t* ids;        // [B, G]
+  const int32_t* draft_len;  // [B] or nullptr
+  const float* uniforms;     // [B, G+1]
+  float scale;               // log2(e) / T
+  int B, G, V;
+  int L;                     // vocabulary slice per CTA (multiple of 8)
+  int vec;                   // every logit row starts on a 16-byte boundary
+  int32_t* emitted;          // [B, G+1]
+  int32_t* n_acc;            // [B]
+  float* beta;               // [B, G] statistics outputs (any may be nullptr)
+  float* p_draft;
+  float* q_draft;
+  float* accept_prob;
+  float* resid;
+  Workspace ws;
+};
+
+struct GreedyParams {
+  const void* target;        // [B, G+1, V]
+  const int32_t* ids;        // [B, G]
+  const int32_t* draft_len;  // [B] or nullptr
+  int B, G, V;
+  int slice;                 // target elements per CTA (multiple of 8)
+  int nslices;               // CTAs per target row
+  int vec;
+  int32_t* emitted;
+  int32_t* n_acc;
+  Workspace ws;
+};
+
+// dtype: 0 = float32, 1 = bfloat16.  stats selects the statistics kernel.
+cudaError_t verify_prepare(int dtype, bool stats, int smem);
+cudaError_t verify_max_active_clusters(int dtype, bool stats, int cs, int smem, int* out);
+cudaError_t verify_launch(const VerifyParams& p, int dtype, bool stats, int cs, int smem, cudaStream_t stream);
+cudaError_t greedy_launch(const GreedyParams& p, int dtype, cudaStream_t stream);
+
+}  // namespace specv

@@ -1,0 +1,94 @@
+"""Comparison of the CUDA path with the float64 oracle on the same seeded inputs.
+
+Tolerances (also derived in the design notes):
+  - tokens and n_accepted: bit-exact, except rows the oracle flags as boundary
+    draws (a tested uniform within 1e-5 of its acceptance threshold, or the
+    final uniform within 1e-5 of a CDF edge); those are counted, and the GPU
+    output of such a row must still be well formed;
+  - greedy: bit-exact, no exemption;
+  - statistics p(x), q(x), min(1, p/q): relative 1e-5 (float32 logits) or 2e-3
+    (bfloat16 logits), plus 1e-37 absolute for values in float32's subnormal
+    range; beta and the residual mass: the same relative bound plus 1e-6
+    absolute, the float32 rounding of sums over V terms of p and q
+    (sum of |p - q| errors <= a few ulp x sum(p + q) = 2).
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle as O
+import workloads as W
+
+RTOL = {"f32": 1e-5, "bf16": 2e-3}
+ATOL_POINT = 1e-37
+ATOL_SUM = 1e-6
+
+
+def host_inputs(w: W.Workload):
+    return dict(target=W.logits_as_numpy(w.target), draft=W.logits_as_numpy(w.draft), dtype=w.dtype,
+                ids=w.ids.cpu().numpy(), draft_len=None if w.draft_len is None else w.draft_len.cpu().numpy(),
+                uniforms=w.uniforms.cpu().numpy(), T=w.T)
+
+
+def check_well_formed(em_row, n, ids_row, gb, V):
+    assert 0 <= n <= gb
+    assert list(em_row[:n]) == list(ids_row[:n])
+    assert 0 <= em_row[n] < V
+    assert (em_row[n + 1:] == -1).all()
+
+
+def compare_sample(w: W.Workload, emitted: torch.Tensor, n_acc: torch.Tensor, h=None, rows=None):
+    """Returns (number compared, boundary rows, mismatched rows)."""
+    h = h or host_inputs(w)
+    ref = O.verify_sample(h["target"], h["draft"], h["dtype"], h["ids"], h["draft_len"], h["uniforms"], h["T"],
+                          rows=rows)
+    em = emitted.cpu().numpy()
+    na = n_acc.cpu().numpy()
+    gl = h["draft_len"] if h["draft_len"] is not None else np.full(w.B, w.gamma)
+    mism, flagged, n = [], [], 0
+    for b in (range(w.B) if rows is None else rows):
+        n += 1
+        if ref["boundary"][b]:
+            flagged.append(b)
+            if ref["valid"][b]:
+                check_well_formed(em[b], int(na[b]), h["ids"][b], int(gl[b]), w.V)
+            continue
+        if int(na[b]) != int(ref["n_accepted"][b]) or list(em[b]) != list(ref["emitted"][b]):
+            mism.append((b, int(na[b]), list(em[b]), int(ref["n_accepted"][b]), list(ref["emitted"][b])))
+    return n, flagged, mism
+
+
+def compare_greedy(w: W.Workload, ids: torch.Tensor, emitted, n_acc, h=None, rows=None):
+    h = h or host_inputs(w)
+    ref = O.verify_greedy(h["target"], h["dtype"], ids.cpu().numpy(), h["draft_len"], rows=rows)
+    em = emitted.cpu().numpy()
+    na = n_acc.cpu().numpy()
+    mism = []
+    for b in (range(w.B) if rows is None else rows):
+        if int(na[b]) != int(ref["n_accepted"][b]) or list(em[b]) != list(ref["emitted"][b]):
+            mism.append((b, int(na[b]), list(em[b]), int(ref["n_accepted"][b]), list(ref["emitted"][b])))
+    return mism
+
+
+def compare_stats(w: W.Workload, st: dict, h=None, rows=None):
+    """Max normalised error per statistic (<= 1 passes) and the number of positions compared."""
+    h = h or host_inputs(w)
+    ref = O.accept_stats(h["target"], h["draft"], h["dtype"], h["ids"], h["draft_len"], h["T"], rows=rows)
+    rtol = RTOL[w.dtype]
+    names = {"beta": "beta", "p_x": "p_x", "q_x": "q_x", "accept_prob": "accept_prob", "resid": "resid"}
+    sel = np.zeros((w.B, w.gamma), dtype=bool)
+    for b in (range(w.B) if rows is None else rows):
+        sel[b] = True
+    worst = {}
+    for k, rk in names.items():
+        g = st[k].cpu().numpy().astype(np.float64)
+        o = ref[rk]
+        valid = ref["valid"] & sel
+        atol = ATOL_SUM if k in ("beta", "resid") else ATOL_POINT
+        err = np.abs(g[valid] - o[valid]) / (rtol * np.abs(o[valid]) + atol)
+        worst[k] = float(err.max()) if err.size else 0.0
+        # positions the oracle does not compute are NaN on both sides
+        inval = sel & ~ref["valid"]
+        assert np.isnan(g[inval]).all(), k
+    return worst, int((ref["valid"] & sel).sum())

@@ -1,0 +1,112 @@
+"""The C-ABI library loads, exports every declared symbol, and rejects bad arguments on the host (CPU only).
+
+No call here reaches a CUDA compute path: every rejected call fails validation
+before the library touches the device.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import speculative_decoding_verification_40_gb300 as S
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h")]
+
+
+def declared_functions():
+    names = []
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^[A-Za-z_][\w\s\*]*?\b(spec_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_functions()
+    assert "spec_verify_sample" in names and "spec_verify_greedy" in names and "spec_accept_stats" in names
+    lib = ctypes.CDLL(S.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_workspace_size():
+    assert S.lib.spec_workspace_size(64, 8, 128256, 1) >= 256 + 64 * 4 + 64 * 9 * 16
+    assert S.lib.spec_workspace_size(-1, 8, 100, 0) == 0
+    assert S.lib.spec_workspace_size(1, 65, 100, 0) == 0
+    assert S.lib.spec_workspace_size(1, 4, 0, 0) == 0
+    assert S.lib.spec_workspace_size(1, 4, 100, 7) == 0
+
+
+FAKE_WS = ctypes.c_void_p(1 << 20)   # aligned, never dereferenced: validation fails first
+BIG = 1 << 40
+
+
+def sample(**kw):
+    a = dict(t=ctypes.c_void_p(4096), d=ctypes.c_void_p(8192), dtype=0, ids=ctypes.c_void_p(12288), gl=None,
+             u=ctypes.c_void_p(16384), T=1.0, B=2, G=3, V=100, em=ctypes.c_void_p(20480),
+             na=ctypes.c_void_p(24576), ws=FAKE_WS, wsb=BIG, st=None)
+    a.update(kw)
+    return S.lib.spec_verify_sample(a["t"], a["d"], a["dtype"], a["ids"], a["gl"], a["u"], a["T"], a["B"], a["G"],
+                                    a["V"], a["em"], a["na"], a["ws"], a["wsb"], a["st"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dtype=3), 2),
+    (dict(B=-1), 1),
+    (dict(G=65), 1),
+    (dict(G=-1), 1),
+    (dict(V=0), 1),
+    (dict(V=262145), 1),
+    (dict(ws=None), 7),
+    (dict(ws=ctypes.c_void_p((1 << 20) + 8)), 7),
+    (dict(wsb=16), 7),
+    (dict(T=0.0), 1),
+    (dict(T=-1.0), 1),
+    (dict(T=float("nan")), 1),
+    (dict(T=float("inf")), 1),
+    (dict(t=None), 1),
+    (dict(d=None), 1),
+    (dict(ids=None), 1),
+    (dict(u=None), 1),
+    (dict(em=None), 1),
+    (dict(na=None), 1),
+])
+def test_sample_rejects_bad_arguments_on_the_host(kw, code):
+    assert sample(**kw) == code
+
+
+def test_empty_batch_is_a_no_op():
+    assert sample(B=0, t=None, d=None, ids=None, u=None, em=None, na=None, ws=None) == 0
+
+
+def test_greedy_and_stats_reject_bad_arguments():
+    L = S.lib
+    assert L.spec_verify_greedy(None, None, 0, ctypes.c_void_p(64), None, 1, 2, 10, ctypes.c_void_p(64),
+                                ctypes.c_void_p(64), FAKE_WS, BIG, None) == 1
+    assert L.spec_verify_greedy(ctypes.c_void_p(64), None, 9, None, None, 1, 2, 10, None, None, FAKE_WS, BIG,
+                                None) == 2
+    assert L.spec_accept_stats(ctypes.c_void_p(64), ctypes.c_void_p(64), 0, ctypes.c_void_p(64), None, 0.0, 1, 2,
+                               10, None, None, None, None, None, FAKE_WS, BIG, None) == 1
+    assert L.spec_accept_stats(None, None, 1, None, None, 1.0, 0, 2, 10, None, None, None, None, None, None, 0,
+                               None) == 0
+
+
+def test_status_strings():
+    for code in range(8):
+        assert S.lib.spec_status_string(code).decode() == S.STATUS[code]
+
+
+@pytest.mark.parametrize("B,G,V,bf16,cs", [(1, 4, 1024, 0, 1), (8, 4, 32128, 1, 4), (64, 8, 128256, 1, 16),
+                                           (256, 5, 152064, 0, 16), (1024, 8, 32000, 1, 4)])
+def test_launch_plans_for_the_five_workloads(B, G, V, bf16, cs, monkeypatch):
+    monkeypatch.delenv("SPECVERIFY_CLUSTER", raising=False)
+    import torch
+    p = S.plan(B, G, V, torch.bfloat16 if bf16 else torch.float32)
+    assert p["cluster_size"] == cs
+    assert p["slice_len"] * cs >= V and p["slice_len"] % 8 == 0
+    assert p["smem_bytes"] <= 227 * 1024

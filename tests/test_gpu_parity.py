@@ -1,0 +1,152 @@
+"""CUDA path vs the float64 oracle on the five seeded workloads at their full sizes (GPU).
+
+Every call goes through the C ABI (via the ctypes binding) in the launch
+configuration the bench times.  Sampling is token-exact outside counted
+boundary draws, greedy is bit-exact, statistics agree within tests/parity.py's
+tolerances.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from parity import compare_greedy, compare_sample, compare_stats, host_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def S():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import speculative_decoding_verification_40_gb300 as S
+    return S
+
+
+def _report(name, n, flagged, mism):
+    print(f"{name}: compared {n} rows, boundary draws {len(flagged)}, mismatches {len(mism)}")
+
+
+@pytest.mark.parametrize("k", [1, 2, 3, 4])
+def test_sample_parity_full_config(S, k):
+    w = W.make(k, device="cuda")
+    em, na = S.verify_sample(w.target, w.draft, w.ids, w.uniforms, w.T, w.draft_len)
+    assert S.check_status() == 0
+    n, flagged, mism = compare_sample(w, em, na)
+    _report(w.name, n, flagged, mism)
+    assert not mism, mism[:5]
+    assert len(flagged) <= max(2, n // 50)
+
+
+def test_sample_parity_c0_many_calls(S):
+    total_flagged = 0
+    for call in range(0, 1000, 20):   # 50 of the 1000 independent calls
+        w = W.make(0, device="cuda", call=call)
+        em, na = S.verify_sample(w.target, w.draft, w.ids, w.uniforms, w.T)
+        n, flagged, mism = compare_sample(w, em, na)
+        assert not mism, (call, mism)
+        total_flagged += len(flagged)
+    assert S.check_status() == 0
+    assert total_flagged <= 2
+
+
+@pytest.mark.parametrize("k", [1, 2, 3, 4])
+def test_greedy_parity_full_config(S, k):
+    w = W.make(k, device="cuda")
+    em, na = S.verify_greedy(w.target, w.greedy_ids, w.draft_len)
+    assert S.check_status() == 0
+    mism = compare_greedy(w, w.greedy_ids, em, na)
+    assert not mism, mism[:5]
+    # sampled drafts as guesses too: mostly early mismatches
+    em, na = S.verify_greedy(w.target, w.ids, w.draft_len)
+    assert not compare_greedy(w, w.ids, em, na)
+
+
+@pytest.mark.parametrize("k", [0, 1, 2, 3, 4])
+def test_stats_parity_full_config(S, k):
+    w = W.make(k, device="cuda")
+    st = S.accept_stats(w.target, w.draft, w.ids, w.T, w.draft_len)
+    assert S.check_status() == 0
+    worst, n = compare_stats(w, st)
+    print(w.name, n, worst)
+    assert n > 0
+    for key, v in worst.items():
+        assert v <= 1.0, (key, v)
+
+
+def test_c2_acceptance_rate_is_near_08(S):
+    """The c2 recipe promises mean beta ~ 0.8 per row (sigma calibrated by the oracle)."""
+    w = W.make(2, device="cuda")
+    st = S.accept_stats(w.target, w.draft, w.ids, w.T)
+    beta = st["beta"].mean(dim=1).cpu().numpy()
+    assert np.all(np.abs(beta - 0.8) < 0.02), beta
+
+
+def test_c4_special_rows(S):
+    """p == q rows accept everything; disjoint rows accept nothing; one-hot targets emit the hot token."""
+    w = W.make(4, device="cuda")
+    em, na = S.verify_sample(w.target, w.draft, w.ids, w.uniforms, w.T, w.draft_len)
+    em, na = em.cpu(), na.cpu()
+    gl = w.draft_len.cpu()
+    kind = w.row_kind.cpu()
+    hot = w.meta["hot"]
+    oh_rows = (kind == W.ROW_ONE_HOT).nonzero().flatten().tolist()
+    for b in range(w.B):
+        gb = int(gl[b])
+        if kind[b] == W.ROW_P_EQ_Q:
+            assert int(na[b]) == gb
+        elif kind[b] == W.ROW_DISJOINT:
+            assert int(na[b]) == 0
+        elif kind[b] == W.ROW_ONE_HOT:
+            n = int(na[b])
+            assert int(em[b, n]) == int(hot[oh_rows.index(b), n])
+    st = S.accept_stats(w.target, w.draft, w.ids, w.T, w.draft_len)
+    beta = st["beta"].cpu()
+    for b in range(w.B):
+        gb = int(gl[b])
+        if kind[b] == W.ROW_P_EQ_Q:
+            assert (beta[b, :gb] == 1.0).all() or torch.allclose(beta[b, :gb], torch.ones(gb), atol=1e-6)
+            assert (st["resid"].cpu()[b, :gb] == 0).all()
+            assert (st["accept_prob"].cpu()[b, :gb] == 1.0).all()
+        elif kind[b] == W.ROW_DISJOINT:
+            assert (beta[b, :gb] == 0).all()
+
+
+def test_repeated_calls_are_identical_and_workspace_resets(S):
+    w = W.make(1, device="cuda")
+    a = S.verify_sample(w.target, w.draft, w.ids, w.uniforms, w.T)
+    g = S.verify_greedy(w.target, w.greedy_ids)
+    b = S.verify_sample(w.target, w.draft, w.ids, w.uniforms, w.T)
+    g2 = S.verify_greedy(w.target, w.greedy_ids)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    assert torch.equal(g[0], g2[0]) and torch.equal(g[1], g2[1])
+    ws = S.workspace_for(torch.device("cuda"), 0)
+    # every counter, record slot and key the calls used is zero again (error word included)
+    nbytes = S.workspace_size(w.B, w.gamma, w.V)
+    head = ws[:256].cpu()
+    assert int(head[:4].view(torch.int32).item()) == 0
+    tickets = ws[256:256 + 4 * w.B].cpu().view(torch.int32)
+    assert int(tickets.abs().sum()) == 0
+    assert nbytes > 0
+
+
+def test_cluster_sizes_agree(S, monkeypatch):
+    """Every cluster size (vocabulary split) gives the oracle's tokens on the same inputs."""
+    w = W.make(1, device="cuda", B=16)
+    h = host_inputs(w)
+    outs = []
+    for cs in (1, 2, 4, 8, 16):
+        if cs == 1 and w.V * 8 > 220 * 1024:
+            continue
+        monkeypatch.setenv("SPECVERIFY_CLUSTER", str(cs))
+        em, na = S.verify_sample(w.target, w.draft, w.ids, w.uniforms, w.T)
+        st = S.accept_stats(w.target, w.draft, w.ids, w.T)
+        n, flagged, mism = compare_sample(w, em, na, h)
+        assert not mism, (cs, mism[:3])
+        worst, _ = compare_stats(w, st, h)
+        assert max(worst.values()) <= 1.0, (cs, worst)
+        outs.append(em.cpu())
+    assert S.check_status() == 0
