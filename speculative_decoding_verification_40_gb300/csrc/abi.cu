@@ -158,7 +158,7 @@ int check_common(int dtype, int B, int gamma, int V, const void* workspace, size
   const int st = check_sizes(dtype, B, gamma, V);
   if (st != SPEC_OK || B == 0) return st;
   if (workspace == nullptr || reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return SPEC_ERR_WORKSPACE;
-  if (ws_bytes < specv::ws_bytes_for(B, gamma)) return SPEC_ERR_WORKSPACE;
+  if (ws_bytes < specv::ws_bytes_for(B, gamma, V)) return SPEC_ERR_WORKSPACE;
   return SPEC_OK;
 }
 
@@ -179,11 +179,32 @@ int run_verify(const void* target, const void* draft, int dtype, const int32_t* 
   if (target == nullptr) return SPEC_ERR_ARG;
   if (gamma > 0 && (draft == nullptr || ids == nullptr)) return SPEC_ERR_ARG;
   if (!stats && (uniforms == nullptr || emitted == nullptr || n_accepted == nullptr)) return SPEC_ERR_ARG;
+  const int esz = dtype == SPEC_F32 ? 4 : 2;
+  const bool vec = rows_aligned(target, V, esz) && (gamma == 0 || rows_aligned(draft, V, esz));
+
+  if (!stats) {
+    specv::SampleParams p = {};
+    p.target = target;
+    p.draft = draft;
+    p.ids = ids;
+    p.draft_len = draft_len;
+    p.uniforms = uniforms;
+    p.scale = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+    p.B = B;
+    p.G = gamma;
+    p.V = V;
+    p.slice = specv::kStreamSlice;
+    p.nslices = specv::stream_slices(V);
+    p.vec = vec ? 1 : 0;
+    p.emitted = emitted;
+    p.n_acc = n_accepted;
+    p.ws = specv::ws_carve(workspace, B, gamma, V);
+    return launch_status(specv::sample_launch(p, dtype, static_cast<cudaStream_t>(stream)));
+  }
 
   Plan plan;
   if ((st = resolve_plan(V, dtype, stats, &plan)) != SPEC_OK) return st;
 
-  const int esz = dtype == SPEC_F32 ? 4 : 2;
   specv::VerifyParams p = {};
   p.target = target;
   p.draft = draft;
@@ -195,7 +216,7 @@ int run_verify(const void* target, const void* draft, int dtype, const int32_t* 
   p.G = gamma;
   p.V = V;
   p.L = plan.L;
-  p.vec = rows_aligned(target, V, esz) && (gamma == 0 || rows_aligned(draft, V, esz)) ? 1 : 0;
+  p.vec = vec ? 1 : 0;
   p.emitted = emitted;
   p.n_acc = n_accepted;
   p.beta = beta;
@@ -203,7 +224,7 @@ int run_verify(const void* target, const void* draft, int dtype, const int32_t* 
   p.q_draft = q_draft;
   p.accept_prob = accept_prob;
   p.resid = resid;
-  p.ws = specv::ws_carve(workspace, B, gamma);
+  p.ws = specv::ws_carve(workspace, B, gamma, V);
   return launch_status(
       specv::verify_launch(p, dtype, stats, plan.cs, plan.smem, static_cast<cudaStream_t>(stream)));
 }
@@ -215,7 +236,7 @@ extern "C" {
 size_t spec_workspace_size(int B, int gamma, int V, int dtype) {
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return 0;
   if (B < 0 || gamma < 0 || gamma > SPEC_MAX_GAMMA || V < 1 || V > SPEC_MAX_VOCAB) return 0;
-  return specv::ws_bytes_for(B, gamma);
+  return specv::ws_bytes_for(B, gamma, V);
 }
 
 int spec_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
@@ -262,7 +283,7 @@ int spec_verify_greedy(const void* target_logits, const void* draft_logits, int 
   p.vec = rows_aligned(target_logits, V, esz) ? 1 : 0;
   p.emitted = emitted;
   p.n_acc = n_accepted;
-  p.ws = specv::ws_carve(workspace, B, gamma);
+  p.ws = specv::ws_carve(workspace, B, gamma, V);
   return launch_status(specv::greedy_launch(p, dtype, static_cast<cudaStream_t>(stream)));
 }
 

@@ -14,6 +14,10 @@ constexpr int kChunk = 128;            // elements per warp-chunk: 32 lanes x 4 
 constexpr int kMaxCluster = 16;        // largest thread-block cluster (non-portable size)
 constexpr int kGreedyThreads = 256;    // threads per CTA of the greedy kernel
 constexpr int kGreedySlice = 8192;     // target-row elements per greedy CTA
+constexpr int kStreamThreads = 256;    // threads per CTA of the streaming sampling kernel
+constexpr int kStreamSlice = 8192;     // vocabulary elements per streaming CTA and row
+constexpr int kMaxVocab = 262144;      // SPEC_MAX_VOCAB
+constexpr int kMaxGamma = 64;          // SPEC_MAX_GAMMA
 
 // Device error word: bit k is set for spec_status_t k.
 constexpr uint32_t kErrArg = 1u << 1;
@@ -30,16 +34,21 @@ struct Workspace {
   int32_t* acc;              // [B, G+1] per position: 1 accept, 0 reject, -1 invalid
   int32_t* tok;              // [B, G+1] token drawn if the walk stops at this position
   unsigned long long* key;   // [B, G+1] greedy (value, index) argmax keys
+  float* part;               // [B, G+1, NS] float4 slice normalisers (m_p, S_p, m_q, S_q)
+  float* xl;                 // [B, G] float2 target / draft logit at the draft token
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-__host__ __device__ inline size_t ws_bytes_for(int B, int G) {
+__host__ __device__ inline int stream_slices(int V) { return (V + kStreamSlice - 1) / kStreamSlice; }
+
+__host__ __device__ inline size_t ws_bytes_for(int B, int G, int V) {
   const size_t P = (size_t)B * (size_t)(G + 1);
-  return 256 + align_up((size_t)B * 4, 256) + 2 * align_up(P * 4, 256) + align_up(P * 8, 256);
+  return 256 + align_up((size_t)B * 4, 256) + 2 * align_up(P * 4, 256) + align_up(P * 8, 256) +
+         align_up(P * stream_slices(V) * 16, 256) + align_up((size_t)B * G * 8, 256);
 }
 
-inline Workspace ws_carve(void* base, int B, int G) {
+inline Workspace ws_carve(void* base, int B, int G, int V) {
   const size_t P = (size_t)B * (size_t)(G + 1);
   char* p = static_cast<char*>(base);
   Workspace w;
@@ -52,6 +61,10 @@ inline Workspace ws_carve(void* base, int B, int G) {
   w.tok = reinterpret_cast<int32_t*>(p);
   p += align_up(P * 4, 256);
   w.key = reinterpret_cast<unsigned long long*>(p);
+  p += align_up(P * 8, 256);
+  w.part = reinterpret_cast<float*>(p);
+  p += align_up(P * stream_slices(V) * 16, 256);
+  w.xl = reinterpret_cast<float*>(p);
   return w;
 }
 

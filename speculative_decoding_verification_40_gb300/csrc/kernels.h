@@ -41,10 +41,27 @@ struct GreedyParams {
   Workspace ws;
 };
 
+struct SampleParams {
+  const void* target;        // [B, G+1, V]
+  const void* draft;         // [B, G, V]
+  const int32_t* ids;        // [B, G]
+  const int32_t* draft_len;  // [B] or nullptr
+  const float* uniforms;     // [B, G+1]
+  float scale;               // log2(e) / T
+  int B, G, V;
+  int slice;                 // vocabulary elements per CTA (multiple of 8)
+  int nslices;               // CTAs per row
+  int vec;                   // every logit row starts on a 16-byte boundary
+  int32_t* emitted;          // [B, G+1]
+  int32_t* n_acc;            // [B]
+  Workspace ws;
+};
+
 // dtype: 0 = float32, 1 = bfloat16.  stats selects the statistics kernel.
 cudaError_t verify_prepare(int dtype, bool stats, int smem);
 cudaError_t verify_max_active_clusters(int dtype, bool stats, int cs, int smem, int* out);
 cudaError_t verify_launch(const VerifyParams& p, int dtype, bool stats, int cs, int smem, cudaStream_t stream);
+cudaError_t sample_launch(const SampleParams& p, int dtype, cudaStream_t stream);
 cudaError_t greedy_launch(const GreedyParams& p, int dtype, cudaStream_t stream);
 
 }  // namespace specv

@@ -214,6 +214,11 @@ __device__ void finalize_row(const VerifyParams& a, int b, int gb) {
     for (int j = n + 1; j < G1; ++j) e[j] = -1;
     a.n_acc[b] = n;
   }
+  // leave every slot this row used at zero: workspaces are shared by calls of any shape
+  for (int j = 0; j <= gb; ++j) {
+    a.ws.acc[(size_t)b * G1 + j] = 0;
+    a.ws.tok[(size_t)b * G1 + j] = 0;
+  }
   a.ws.ticket[b] = 0u;
 }
 
