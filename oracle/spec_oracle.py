@@ -105,6 +105,19 @@ def inverse_cdf(w: np.ndarray, u: float):
     return k, bool(flagged)
 
 
+def draw_candidates(w: np.ndarray, u: float) -> list[int]:
+    """Tokens whose normalised CDF cell [C_{k-1}/Z, C_k/Z] (w_k > 0) lies within 1e-5 of u (R8).
+
+    A draw flagged by R8 may land on any of these once the CDF is perturbed by
+    less than 1e-5 of its total; the chosen token of inverse_cdf is always one.
+    """
+    Z = float(np.sum(w))
+    C = np.cumsum(w) / Z
+    lo = np.concatenate([[0.0], C[:-1]])
+    ok = (w > 0) & (lo - BOUNDARY_EPS <= u) & (u <= C + BOUNDARY_EPS)
+    return [int(k) for k in np.nonzero(ok)[0]]
+
+
 def verify_row(tl: np.ndarray, dl: np.ndarray, ids: np.ndarray, gb: int, u: np.ndarray, T: float):
     """Algorithm 1 Phases 3-4 for one row [p1 §2.3; p2 "The algorithm"; p3 §3].
 
@@ -114,7 +127,8 @@ def verify_row(tl: np.ndarray, dl: np.ndarray, ids: np.ndarray, gb: int, u: np.n
     """
     gamma = dl.shape[0]
     V = tl.shape[1]
-    bad = dict(emitted=[-1] * (gamma + 1), n=-1, boundary=False, valid=False)
+    bad = dict(emitted=[-1] * (gamma + 1), n=-1, boundary=False, valid=False, accept_boundary=False,
+               candidates=[])
     if not (0 <= gb <= gamma):
         return bad
     for i in range(gb + 1):
@@ -154,9 +168,12 @@ def verify_row(tl: np.ndarray, dl: np.ndarray, ids: np.ndarray, gb: int, u: np.n
     else:
         w = p[gb]                                  # bonus t ~ p_{gamma+1} [p1 Phase 4]
     tok, flag = inverse_cdf(w, float(u[gamma]))
+    accept_boundary = boundary
     boundary = boundary or flag
     emitted = [int(ids[i]) for i in range(n)] + [tok] + [-1] * (gamma - n)
-    return dict(emitted=emitted, n=n, boundary=boundary, valid=True)
+    cands = draw_candidates(w, float(u[gamma])) if flag else [tok]
+    return dict(emitted=emitted, n=n, boundary=boundary, valid=True, accept_boundary=accept_boundary,
+                candidates=cands)
 
 
 def greedy_row(tl: np.ndarray, ids: np.ndarray, gb: int, gamma: int):
@@ -225,7 +242,9 @@ def verify_sample(target, draft, dtype, ids, draft_len, uniforms, T, rows=None):
     emitted = np.full((B, G1), -2, dtype=np.int64)
     n_acc = np.full(B, -2, dtype=np.int64)
     boundary = np.zeros(B, dtype=bool)
+    accept_boundary = np.zeros(B, dtype=bool)
     valid = np.zeros(B, dtype=bool)
+    candidates = {}
     for b in (range(B) if rows is None else rows):
         gb = int(gl[b])
         tb = widen(target[b], dtype)
@@ -234,8 +253,11 @@ def verify_sample(target, draft, dtype, ids, draft_len, uniforms, T, rows=None):
         emitted[b] = res["emitted"]
         n_acc[b] = res["n"]
         boundary[b] = res["boundary"]
+        accept_boundary[b] = res["accept_boundary"]
         valid[b] = res["valid"]
-    return dict(emitted=emitted, n_accepted=n_acc, boundary=boundary, valid=valid)
+        candidates[b] = res["candidates"]
+    return dict(emitted=emitted, n_accepted=n_acc, boundary=boundary, accept_boundary=accept_boundary,
+                valid=valid, candidates=candidates)
 
 
 def verify_greedy(target, dtype, ids, draft_len, rows=None):

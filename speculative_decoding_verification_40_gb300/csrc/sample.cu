@@ -230,6 +230,10 @@ __device__ void finish_row(const SampleParams& a, int b, int gb, FinishSmem& sm)
   }
   __syncthreads();
   if (err) atomicOr(&sm.err, err);
+  // every partial and logit slot this row used goes back to zero: workspaces are shared by calls of any shape
+  float4* partw = reinterpret_cast<float4*>(a.ws.part) + (size_t)b * G1 * NS;
+  for (int k = tid; k < (gb + 1) * NS; k += kST) partw[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k = tid; k < gb; k += kST) reinterpret_cast<float2*>(a.ws.xl)[(size_t)b * a.G + k] = make_float2(0.f, 0.f);
   __syncthreads();
   if (tid == 0) {
     int n = gb;

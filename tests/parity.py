@@ -53,6 +53,13 @@ def compare_sample(w: W.Workload, emitted: torch.Tensor, n_acc: torch.Tensor, h=
             flagged.append(b)
             if ref["valid"][b]:
                 check_well_formed(em[b], int(na[b]), h["ids"][b], int(gl[b]), w.V)
+                if not ref["accept_boundary"][b]:
+                    # only the final draw is near a CDF edge: same walk, and a token within 1e-5 of the edge
+                    nb = int(ref["n_accepted"][b])
+                    if int(na[b]) != nb or list(em[b][:nb]) != list(ref["emitted"][b][:nb]) or \
+                            int(em[b][nb]) not in ref["candidates"][b]:
+                        mism.append((b, "boundary draw outside the 1e-5 candidates", int(na[b]), list(em[b]),
+                                     nb, ref["candidates"][b]))
             continue
         if int(na[b]) != int(ref["n_accepted"][b]) or list(em[b]) != list(ref["emitted"][b]):
             mism.append((b, int(na[b]), list(em[b]), int(ref["n_accepted"][b]), list(ref["emitted"][b])))

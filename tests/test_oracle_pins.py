@@ -330,3 +330,14 @@ def test_batched_wrappers_match_rows():
                 assert np.isfinite(st["beta"][b, i])
             else:
                 assert np.isnan(st["beta"][b, i])
+
+
+def test_draw_candidates_cover_the_near_edge_tokens():
+    w = np.array([0.5, 1e-7, 0.0, 0.4999999, 1e-6])
+    Z = w.sum()
+    u = 0.5 / Z                       # exactly the upper edge of token 0
+    c = O.draw_candidates(w, u)
+    assert 0 in c and 1 in c and 3 in c and 2 not in c
+    k, flag = O.inverse_cdf(w, u)
+    assert flag and k in c
+    assert O.draw_candidates(w, 0.25) == [0]
