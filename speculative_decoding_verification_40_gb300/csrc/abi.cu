@@ -26,7 +26,7 @@ struct Plan {
 
 int smem_for(int L) {
   const int Lpad = static_cast<int>(align_up(L, specv::kChunk));
-  return 2 * Lpad * 4 + 2 * (Lpad / specv::kChunk) * 4;
+  return 2 * Lpad * 4;
 }
 
 Plan plan_for(int V, int cs) {
@@ -68,27 +68,67 @@ bool choose_plan(int V, Plan* out) {
 }
 
 // Kernel attributes are per device; set them once per (device, kernel, dtype).
-std::atomic<int> g_prepared[kMaxDevices][2][2];
+std::atomic<int> g_prepared[kMaxDevices][2];
 std::mutex g_prep_mu;
 
-int prepare(int dtype, bool stats) {
+int prepare(int dtype) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPEC_ERR_CUDA;
-  std::atomic<int>& flag = g_prepared[dev][dtype][stats ? 1 : 0];
+  std::atomic<int>& flag = g_prepared[dev][dtype];
   if (flag.load(std::memory_order_acquire)) return SPEC_OK;
   std::lock_guard<std::mutex> lk(g_prep_mu);
   if (!flag.load(std::memory_order_relaxed)) {
-    if (specv::verify_prepare(dtype, stats, kSmemMax) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (specv::stats_prepare(dtype, kSmemMax) != cudaSuccess) return SPEC_ERR_CUDA;
     flag.store(1, std::memory_order_release);
   }
   return SPEC_OK;
 }
 
+// Grid of the persistent sampling kernel: every CTA the device can hold at once (cooperative launch).
+std::atomic<int> g_sample_grid[kMaxDevices][2];
+
+int sample_grid(int dtype, int* grid) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPEC_ERR_CUDA;
+  int g = g_sample_grid[dev][dtype].load(std::memory_order_acquire);
+  if (g == 0) {
+    int sms = 0, per = 0, coop = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess ||
+        specv::sample_occupancy(dtype, &per) != cudaSuccess) {
+      cudaGetLastError();
+      return SPEC_ERR_CUDA;
+    }
+    if (!coop || per < 1) return SPEC_ERR_CUDA;
+    g = sms * per;
+    g_sample_grid[dev][dtype].store(g, std::memory_order_release);
+  }
+  *grid = g;
+  return SPEC_OK;
+}
+
+// Vocabulary elements per sampling work item: 32 KB of one logit row, at least V/32 so a row has
+// at most 32 slices; SPECVERIFY_SLICE (elements) overrides within the same limits.
+int sample_slice(int V, int dtype) {
+  const int chunk = 32 * (dtype == SPEC_F32 ? 4 : 8);  // elements per 32-lane chunk
+  const int esz = dtype == SPEC_F32 ? 4 : 2;
+  int slice = specv::kStreamSliceBytes / esz;
+  if (const char* env = std::getenv("SPECVERIFY_SLICE")) {
+    const int want = std::atoi(env);
+    if (want > 0) slice = want;
+  }
+  const int lo = (V + specv::kMaxSlices - 1) / specv::kMaxSlices;
+  if (slice < lo) slice = lo;
+  slice = static_cast<int>(align_up(slice, chunk));
+  if (slice > specv::kMaxChunksPerSlice * chunk) slice = specv::kMaxChunksPerSlice * chunk;
+  return slice;
+}
+
 // Falls back to smaller clusters when the device cannot co-schedule the planned one.
-int schedulable_plan(int V, int dtype, bool stats, Plan* plan) {
+int schedulable_plan(int V, int dtype, Plan* plan) {
   for (int tries = 0; tries < 5; ++tries) {
     int n = 0;
-    if (specv::verify_max_active_clusters(dtype, stats, plan->cs, plan->smem, &n) != cudaSuccess) {
+    if (specv::stats_max_active_clusters(dtype, plan->cs, plan->smem, &n) != cudaSuccess) {
       cudaGetLastError();
       return SPEC_ERR_CUDA;
     }
@@ -103,7 +143,7 @@ int schedulable_plan(int V, int dtype, bool stats, Plan* plan) {
 
 // Plans already resolved on a device (the occupancy query costs tens of microseconds).
 struct PlanEntry {
-  int dev, V, dtype, stats, env_cs;
+  int dev, V, dtype, env_cs;
   Plan plan;
 };
 std::mutex g_plan_mu;
@@ -114,7 +154,7 @@ int env_cluster() {
   return env ? std::atoi(env) : 0;
 }
 
-int resolve_plan(int V, int dtype, bool stats, Plan* out) {
+int resolve_plan(int V, int dtype, Plan* out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
@@ -124,7 +164,7 @@ int resolve_plan(int V, int dtype, bool stats, Plan* out) {
   {
     std::lock_guard<std::mutex> lk(g_plan_mu);
     for (const PlanEntry& e : g_plans) {
-      if (e.dev == dev && e.V == V && e.dtype == dtype && e.stats == (stats ? 1 : 0) && e.env_cs == env_cs) {
+      if (e.dev == dev && e.V == V && e.dtype == dtype && e.env_cs == env_cs) {
         *out = e.plan;
         return SPEC_OK;
       }
@@ -132,11 +172,11 @@ int resolve_plan(int V, int dtype, bool stats, Plan* out) {
   }
   Plan plan;
   if (!choose_plan(V, &plan)) return SPEC_ERR_ARG;
-  int st = prepare(dtype, stats);
+  int st = prepare(dtype);
   if (st != SPEC_OK) return st;
-  if ((st = schedulable_plan(V, dtype, stats, &plan)) != SPEC_OK) return st;
+  if ((st = schedulable_plan(V, dtype, &plan)) != SPEC_OK) return st;
   std::lock_guard<std::mutex> lk(g_plan_mu);
-  if (g_plans.size() < 4096) g_plans.push_back(PlanEntry{dev, V, dtype, stats ? 1 : 0, env_cs, plan});
+  if (g_plans.size() < 4096) g_plans.push_back(PlanEntry{dev, V, dtype, env_cs, plan});
   *out = plan;
   return SPEC_OK;
 }
@@ -183,6 +223,8 @@ int run_verify(const void* target, const void* draft, int dtype, const int32_t* 
   const bool vec = rows_aligned(target, V, esz) && (gamma == 0 || rows_aligned(draft, V, esz));
 
   if (!stats) {
+    int grid = 0;
+    if ((st = sample_grid(dtype, &grid)) != SPEC_OK) return st;
     specv::SampleParams p = {};
     p.target = target;
     p.draft = draft;
@@ -193,40 +235,45 @@ int run_verify(const void* target, const void* draft, int dtype, const int32_t* 
     p.B = B;
     p.G = gamma;
     p.V = V;
-    p.slice = specv::kStreamSlice;
-    p.nslices = specv::stream_slices(V);
+    p.slice = sample_slice(V, dtype);
+    p.nslices = (V + p.slice - 1) / p.slice;
+    // draw items of row b are taken about two grid-rounds of items after its stream items (three for
+    // ragged batches, whose padded positions are empty items): the row is decided by then, and its
+    // rows are still in L2
+    const long long unit = (long long)(gamma + 2) * p.nslices;
+    const long long rounds = draft_len ? 3 : 2;
+    const long long lag = (rounds * grid + unit - 1) / unit;
+    p.lag = static_cast<int>(lag < 1 ? 1 : (lag > B ? B : lag));
     p.vec = vec ? 1 : 0;
     p.emitted = emitted;
     p.n_acc = n_accepted;
     p.ws = specv::ws_carve(workspace, B, gamma, V);
-    return launch_status(specv::sample_launch(p, dtype, static_cast<cudaStream_t>(stream)));
+    const long long items = (long long)B * (gamma + 1) * p.nslices + (long long)B * p.nslices;
+    if (items < grid) grid = static_cast<int>(items);
+    return launch_status(specv::sample_launch(p, dtype, grid, static_cast<cudaStream_t>(stream)));
   }
 
   Plan plan;
-  if ((st = resolve_plan(V, dtype, stats, &plan)) != SPEC_OK) return st;
+  if ((st = resolve_plan(V, dtype, &plan)) != SPEC_OK) return st;
 
   specv::VerifyParams p = {};
   p.target = target;
   p.draft = draft;
   p.ids = ids;
   p.draft_len = draft_len;
-  p.uniforms = uniforms;
   p.scale = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
   p.B = B;
   p.G = gamma;
   p.V = V;
   p.L = plan.L;
   p.vec = vec ? 1 : 0;
-  p.emitted = emitted;
-  p.n_acc = n_accepted;
   p.beta = beta;
   p.p_draft = p_draft;
   p.q_draft = q_draft;
   p.accept_prob = accept_prob;
   p.resid = resid;
   p.ws = specv::ws_carve(workspace, B, gamma, V);
-  return launch_status(
-      specv::verify_launch(p, dtype, stats, plan.cs, plan.smem, static_cast<cudaStream_t>(stream)));
+  return launch_status(specv::stats_launch(p, dtype, plan.cs, plan.smem, static_cast<cudaStream_t>(stream)));
 }
 
 }  // namespace
@@ -313,7 +360,7 @@ int spec_verify_plan(int B, int gamma, int V, int dtype, int* cluster_size, int*
   Plan plan;
   int dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess) {
-    if ((st = resolve_plan(V, dtype, false, &plan)) != SPEC_OK) return st;
+    if ((st = resolve_plan(V, dtype, &plan)) != SPEC_OK) return st;
   } else {
     cudaGetLastError();  // no device: report the plan before the co-scheduling check
     if (!choose_plan(V, &plan)) return SPEC_ERR_ARG;

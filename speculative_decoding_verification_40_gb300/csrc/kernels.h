@@ -13,13 +13,10 @@ struct VerifyParams {
   const void* draft;         // [B, G, V]
   const int32_t* ids;        // [B, G]
   const int32_t* draft_len;  // [B] or nullptr
-  const float* uniforms;     // [B, G+1]
   float scale;               // log2(e) / T
   int B, G, V;
   int L;                     // vocabulary slice per CTA (multiple of 8)
   int vec;                   // every logit row starts on a 16-byte boundary
-  int32_t* emitted;          // [B, G+1]
-  int32_t* n_acc;            // [B]
   float* beta;               // [B, G] statistics outputs (any may be nullptr)
   float* p_draft;
   float* q_draft;
@@ -49,8 +46,9 @@ struct SampleParams {
   const float* uniforms;     // [B, G+1]
   float scale;               // log2(e) / T
   int B, G, V;
-  int slice;                 // vocabulary elements per CTA (multiple of 8)
-  int nslices;               // CTAs per row
+  int slice;                 // vocabulary elements per work item (a multiple of 32 x elements per 16 bytes)
+  int nslices;               // work items per logit row (<= kMaxSlices)
+  int lag;                   // draw items of row b follow the stream items of row b + lag
   int vec;                   // every logit row starts on a 16-byte boundary
   int32_t* emitted;          // [B, G+1]
   int32_t* n_acc;            // [B]
@@ -58,10 +56,11 @@ struct SampleParams {
 };
 
 // dtype: 0 = float32, 1 = bfloat16.  stats selects the statistics kernel.
-cudaError_t verify_prepare(int dtype, bool stats, int smem);
-cudaError_t verify_max_active_clusters(int dtype, bool stats, int cs, int smem, int* out);
-cudaError_t verify_launch(const VerifyParams& p, int dtype, bool stats, int cs, int smem, cudaStream_t stream);
-cudaError_t sample_launch(const SampleParams& p, int dtype, cudaStream_t stream);
+cudaError_t stats_prepare(int dtype, int smem);
+cudaError_t stats_max_active_clusters(int dtype, int cs, int smem, int* out);
+cudaError_t stats_launch(const VerifyParams& p, int dtype, int cs, int smem, cudaStream_t stream);
+cudaError_t sample_occupancy(int dtype, int* ctas_per_sm);
+cudaError_t sample_launch(const SampleParams& p, int dtype, int grid, cudaStream_t stream);
 cudaError_t greedy_launch(const GreedyParams& p, int dtype, cudaStream_t stream);
 
 }  // namespace specv
