@@ -84,33 +84,10 @@ int prepare(int dtype) {
   return SPEC_OK;
 }
 
-// Grid of the persistent sampling kernel: every CTA the device can hold at once (cooperative launch).
-std::atomic<int> g_sample_grid[kMaxDevices][2];
-
-int sample_grid(int dtype, int* grid) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPEC_ERR_CUDA;
-  int g = g_sample_grid[dev][dtype].load(std::memory_order_acquire);
-  if (g == 0) {
-    int sms = 0, per = 0, coop = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess ||
-        specv::sample_occupancy(dtype, &per) != cudaSuccess) {
-      cudaGetLastError();
-      return SPEC_ERR_CUDA;
-    }
-    if (!coop || per < 1) return SPEC_ERR_CUDA;
-    g = sms * per;
-    g_sample_grid[dev][dtype].store(g, std::memory_order_release);
-  }
-  *grid = g;
-  return SPEC_OK;
-}
-
-// Vocabulary elements per sampling work item: 32 KB of one logit row, at least V/32 so a row has
+// Vocabulary elements per sampling CTA and logit row: 64 KB of the row, at least V/32 so a row has
 // at most 32 slices; SPECVERIFY_SLICE (elements) overrides within the same limits.
 int sample_slice(int V, int dtype) {
-  const int chunk = 32 * (dtype == SPEC_F32 ? 4 : 8);  // elements per 32-lane chunk
+  const int chunk = 4 * 32 * (dtype == SPEC_F32 ? 4 : 8);  // elements per draw chunk (4 x 32 lanes x 16 B)
   const int esz = dtype == SPEC_F32 ? 4 : 2;
   int slice = specv::kStreamSliceBytes / esz;
   if (const char* env = std::getenv("SPECVERIFY_SLICE")) {
@@ -223,8 +200,6 @@ int run_verify(const void* target, const void* draft, int dtype, const int32_t* 
   const bool vec = rows_aligned(target, V, esz) && (gamma == 0 || rows_aligned(draft, V, esz));
 
   if (!stats) {
-    int grid = 0;
-    if ((st = sample_grid(dtype, &grid)) != SPEC_OK) return st;
     specv::SampleParams p = {};
     p.target = target;
     p.draft = draft;
@@ -237,20 +212,11 @@ int run_verify(const void* target, const void* draft, int dtype, const int32_t* 
     p.V = V;
     p.slice = sample_slice(V, dtype);
     p.nslices = (V + p.slice - 1) / p.slice;
-    // draw items of row b are taken about two grid-rounds of items after its stream items (three for
-    // ragged batches, whose padded positions are empty items): the row is decided by then, and its
-    // rows are still in L2
-    const long long unit = (long long)(gamma + 2) * p.nslices;
-    const long long rounds = draft_len ? 3 : 2;
-    const long long lag = (rounds * grid + unit - 1) / unit;
-    p.lag = static_cast<int>(lag < 1 ? 1 : (lag > B ? B : lag));
     p.vec = vec ? 1 : 0;
     p.emitted = emitted;
     p.n_acc = n_accepted;
     p.ws = specv::ws_carve(workspace, B, gamma, V);
-    const long long items = (long long)B * (gamma + 1) * p.nslices + (long long)B * p.nslices;
-    if (items < grid) grid = static_cast<int>(items);
-    return launch_status(specv::sample_launch(p, dtype, grid, static_cast<cudaStream_t>(stream)));
+    return launch_status(specv::sample_launch(p, dtype, static_cast<cudaStream_t>(stream)));
   }
 
   Plan plan;

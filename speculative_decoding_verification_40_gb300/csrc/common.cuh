@@ -14,7 +14,7 @@ constexpr int kChunk = 128;            // elements per warp-chunk: 32 lanes x 4 
 constexpr int kMaxCluster = 16;        // largest thread-block cluster (non-portable size)
 constexpr int kGreedyThreads = 256;    // threads per CTA of the greedy kernel
 constexpr int kGreedySlice = 8192;     // target-row elements per greedy CTA
-constexpr int kStreamThreads = 256;    // threads per CTA of the persistent sampling kernel
+constexpr int kStreamThreads = 256;    // threads per CTA of the sampling kernels
 constexpr int kStreamSliceBytes = 65536;  // bytes of one logit row per sampling work item
 constexpr int kMaxVocab = 262144;      // SPEC_MAX_VOCAB
 constexpr int kMaxGamma = 64;          // SPEC_MAX_GAMMA
@@ -33,21 +33,16 @@ constexpr float kZFloor = 1e-15f;
 // returns the slots it used to zero, so workspaces can be shared by calls of
 // any shape.  Only the error word keeps its value until it is read.
 constexpr int kMaxSlices = 32;          // vocabulary slices per row in the sampling kernel
-constexpr int kMaxChunksPerSlice = 128; // 32-lane chunks per sampling slice
+constexpr int kMaxChunksPerSlice = 128; // chunks per sampling slice
 
 struct Workspace {
   uint32_t* err;             // error word (bits above)
-  unsigned long long* fetch; // next work item of the persistent sampling kernel
-  uint32_t* done;            // CTAs of the persistent sampling kernel that have finished
-  uint32_t* ticket;          // [B] stream-item arrivals per batch row (greedy: slice CTAs)
-  uint32_t* dticket;         // [B] draw-item arrivals per batch row
-  uint32_t* ready;           // [B] 1 once the row's accept decisions are published
-  float* rowstate;           // [B] 32-byte draw parameters of each row
+  uint32_t* ticket;          // [B] arrivals per batch row: greedy slice CTAs, or draw CTAs
   unsigned long long* key;   // [B, G+1] greedy (value, index) argmax keys
   float* part;               // [B, G+1, kMaxSlices] float4 slice normalisers (m_p, S_p, m_q, S_q)
   float* xl;                 // [B, G] float2 target / draft logit at the draft token
   float* dsum;               // [B, kMaxSlices] float2 mass of each draw slice (residual, p)
-  float* dch;                // [B, chunks] float2 mass of each 32-lane chunk of the drawn row(s)
+  float* dch;                // [B, chunks] float2 mass of each chunk of the drawn row(s)
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -57,9 +52,9 @@ __host__ __device__ inline size_t chunks_per_row(int V) { return (size_t)(V + 12
 
 __host__ __device__ inline size_t ws_bytes_for(int B, int G, int V) {
   const size_t P = (size_t)B * (size_t)(G + 1);
-  return 256 + 3 * align_up((size_t)B * 4, 256) + align_up((size_t)B * 32, 256) + align_up(P * 8, 256) +
-         align_up(P * kMaxSlices * 16, 256) + align_up((size_t)B * G * 8, 256) +
-         align_up((size_t)B * kMaxSlices * 8, 256) + align_up((size_t)B * chunks_per_row(V) * 8, 256);
+  return 256 + align_up((size_t)B * 4, 256) + align_up(P * 8, 256) + align_up(P * kMaxSlices * 16, 256) +
+         align_up((size_t)B * G * 8, 256) + align_up((size_t)B * kMaxSlices * 8, 256) +
+         align_up((size_t)B * chunks_per_row(V) * 8, 256);
 }
 
 inline Workspace ws_carve(void* base, int B, int G, int V) {
@@ -67,17 +62,9 @@ inline Workspace ws_carve(void* base, int B, int G, int V) {
   char* p = static_cast<char*>(base);
   Workspace w;
   w.err = reinterpret_cast<uint32_t*>(p);
-  w.fetch = reinterpret_cast<unsigned long long*>(p + 128);  // own 128-byte line: every CTA takes items here
-  w.done = reinterpret_cast<uint32_t*>(p + 64);
   p += 256;
   w.ticket = reinterpret_cast<uint32_t*>(p);
   p += align_up((size_t)B * 4, 256);
-  w.dticket = reinterpret_cast<uint32_t*>(p);
-  p += align_up((size_t)B * 4, 256);
-  w.ready = reinterpret_cast<uint32_t*>(p);
-  p += align_up((size_t)B * 4, 256);
-  w.rowstate = reinterpret_cast<float*>(p);
-  p += align_up((size_t)B * 32, 256);
   w.key = reinterpret_cast<unsigned long long*>(p);
   p += align_up(P * 8, 256);
   w.part = reinterpret_cast<float*>(p);

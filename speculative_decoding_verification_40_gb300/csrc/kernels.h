@@ -48,7 +48,6 @@ struct SampleParams {
   int B, G, V;
   int slice;                 // vocabulary elements per work item (a multiple of 32 x elements per 16 bytes)
   int nslices;               // work items per logit row (<= kMaxSlices)
-  int lag;                   // draw items of row b follow the stream items of row b + lag
   int vec;                   // every logit row starts on a 16-byte boundary
   int32_t* emitted;          // [B, G+1]
   int32_t* n_acc;            // [B]
@@ -59,8 +58,7 @@ struct SampleParams {
 cudaError_t stats_prepare(int dtype, int smem);
 cudaError_t stats_max_active_clusters(int dtype, int cs, int smem, int* out);
 cudaError_t stats_launch(const VerifyParams& p, int dtype, int cs, int smem, cudaStream_t stream);
-cudaError_t sample_occupancy(int dtype, int* ctas_per_sm);
-cudaError_t sample_launch(const SampleParams& p, int dtype, int grid, cudaStream_t stream);
+cudaError_t sample_launch(const SampleParams& p, int dtype, cudaStream_t stream);
 cudaError_t greedy_launch(const GreedyParams& p, int dtype, cudaStream_t stream);
 
 }  // namespace specv
