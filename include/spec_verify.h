@@ -101,6 +101,26 @@ int spec_verify_sample(const void* target_logits, const void* draft_logits, int 
                        int32_t* emitted, int32_t* n_accepted,
                        void* workspace, size_t ws_bytes, void* stream);
 
+/* The two phases of spec_verify_sample, for callers that want to schedule them
+ * separately (for instance, the draw phase next to other work on the GPU).
+ * spec_verify_sample_stream reads every logit once and leaves per-slice
+ * softmax normalisers and the logits at the draft tokens in the workspace;
+ * spec_verify_sample_draw takes the accept decisions, draws, writes emitted
+ * and n_accepted, and returns the workspace to its zero state.  Call them in
+ * this order, on the same stream, with identical arguments and workspace, and
+ * nothing else using that workspace in between; together they are exactly
+ * spec_verify_sample.  Arguments, layouts and errors as spec_verify_sample. */
+int spec_verify_sample_stream(const void* target_logits, const void* draft_logits, int dtype,
+                              const int32_t* draft_ids, const int32_t* draft_len, const float* uniforms,
+                              float temperature, int B, int gamma, int V,
+                              int32_t* emitted, int32_t* n_accepted,
+                              void* workspace, size_t ws_bytes, void* stream);
+int spec_verify_sample_draw(const void* target_logits, const void* draft_logits, int dtype,
+                            const int32_t* draft_ids, const int32_t* draft_len, const float* uniforms,
+                            float temperature, int B, int gamma, int V,
+                            int32_t* emitted, int32_t* n_accepted,
+                            void* workspace, size_t ws_bytes, void* stream);
+
 /* Greedy verification: argmax standardisation (paper-graph-ui teardown §2.2;
  * multigrid.ai on sampling temperature).  a_i = argmax_k target[b,i,k], lowest
  * index on ties; guesses are accepted while a_i == draft_ids[b,i]; the emitted

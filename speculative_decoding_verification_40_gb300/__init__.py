@@ -5,7 +5,7 @@ include/spec_verify.h.  The functions here only marshal torch CUDA tensors
 (device pointers, sizes, the current stream) into the C calls: every step of
 the verification runs in the library's CUDA kernels.  Importing this package
 fails if the library has not been built
-(python -m speculative_decoding_verification_40_gb300.build).
+(python speculative_decoding_verification_40_gb300/build.py).
 
 Entry points (same names as the C ABI, without the spec_ prefix):
   verify_sample  -- accept test, first rejection, residual / bonus draw
@@ -41,15 +41,17 @@ class SpecVerifyError(RuntimeError):
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is missing: build it with "
-                          "`python -m speculative_decoding_verification_40_gb300.build`")
+                          "`python speculative_decoding_verification_40_gb300/build.py`")
     L = ctypes.CDLL(LIB_PATH)
     vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     L.spec_workspace_size.argtypes = [i32, i32, i32, i32]
     L.spec_workspace_size.restype = sz
     L.spec_workspace_init.argtypes = [vp, sz, vp]
     L.spec_workspace_init.restype = i32
-    L.spec_verify_sample.argtypes = [vp, vp, i32, vp, vp, vp, f32, i32, i32, i32, vp, vp, vp, sz, vp]
-    L.spec_verify_sample.restype = i32
+    for name in ("spec_verify_sample", "spec_verify_sample_stream", "spec_verify_sample_draw"):
+        fn = getattr(L, name)
+        fn.argtypes = [vp, vp, i32, vp, vp, vp, f32, i32, i32, i32, vp, vp, vp, sz, vp]
+        fn.restype = i32
     L.spec_verify_greedy.argtypes = [vp, vp, i32, vp, vp, i32, i32, i32, vp, vp, vp, sz, vp]
     L.spec_verify_greedy.restype = i32
     L.spec_accept_stats.argtypes = [vp, vp, i32, vp, vp, f32, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]
@@ -169,8 +171,12 @@ def _common(target, draft, ids, draft_len, gamma_needs_draft=True):
 
 def verify_sample(target: torch.Tensor, draft: torch.Tensor, ids: torch.Tensor, uniforms: torch.Tensor,
                   temperature: float, draft_len: torch.Tensor | None = None, *, emitted=None, n_accepted=None,
-                  workspace: torch.Tensor | None = None, check: bool = False):
-    """spec_verify_sample: returns (emitted [B, gamma+1] int32, n_accepted [B] int32)."""
+                  workspace: torch.Tensor | None = None, check: bool = False, phase: str = "both"):
+    """spec_verify_sample: returns (emitted [B, gamma+1] int32, n_accepted [B] int32).
+
+    phase="stream" / "draw" calls spec_verify_sample_stream / spec_verify_sample_draw: the two halves
+    of the same computation, to be called in that order with the same arguments and workspace.
+    """
     B, G, V = _common(target, draft, ids, draft_len)
     _cuda(uniforms, "uniforms", torch.float32, (B, G + 1))
     dev = target.device
@@ -181,10 +187,12 @@ def verify_sample(target: torch.Tensor, draft: torch.Tensor, ids: torch.Tensor, 
     _cuda(emitted, "emitted", torch.int32, (B, G + 1))
     _cuda(n_accepted, "n_accepted", torch.int32, (B,))
     ws = workspace if workspace is not None else workspace_for(dev, workspace_size(B, G, V, target.dtype))
-    code = lib.spec_verify_sample(_p(target), _p(draft) if G > 0 else None, _dtype_code(target),
-                                  _p(ids) if G > 0 else None, _p(draft_len), _p(uniforms), float(temperature),
-                                  B, G, V, _p(emitted), _p(n_accepted), _p(ws), ws.numel(), _stream(dev))
-    _raise(code, "spec_verify_sample")
+    fn = {"both": lib.spec_verify_sample, "stream": lib.spec_verify_sample_stream,
+          "draw": lib.spec_verify_sample_draw}[phase]
+    code = fn(_p(target), _p(draft) if G > 0 else None, _dtype_code(target), _p(ids) if G > 0 else None,
+              _p(draft_len), _p(uniforms), float(temperature), B, G, V, _p(emitted), _p(n_accepted), _p(ws),
+              ws.numel(), _stream(dev))
+    _raise(code, "spec_verify_sample" if phase == "both" else f"spec_verify_sample_{phase}")
     if check:
         check_status(ws)
     return emitted, n_accepted

@@ -1,6 +1,6 @@
 """Builds libspecverify.so (the C-ABI verification library) in-tree with nvcc for sm_103a.
 
-    python -m speculative_decoding_verification_40_gb300.build [--force] [--verbose]
+    python speculative_decoding_verification_40_gb300/build.py [--force] [--verbose]
 
 Each .cu file under csrc/ compiles to an object in _build/ (in parallel), and the
 objects link into libspecverify.so next to this file with the CUDA runtime

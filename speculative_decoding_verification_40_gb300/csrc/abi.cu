@@ -185,10 +185,11 @@ int launch_status(cudaError_t e) {
   return SPEC_ERR_CUDA;
 }
 
+// phases (sampling only): 1 = stream kernel, 2 = draw kernel, 3 = both.
 int run_verify(const void* target, const void* draft, int dtype, const int32_t* ids, const int32_t* draft_len,
                const float* uniforms, float temperature, int B, int gamma, int V, int32_t* emitted,
                int32_t* n_accepted, float* beta, float* p_draft, float* q_draft, float* accept_prob,
-               float* resid, void* workspace, size_t ws_bytes, void* stream, bool stats) {
+               float* resid, void* workspace, size_t ws_bytes, void* stream, bool stats, int phases = 3) {
   int st = check_common(dtype, B, gamma, V, workspace, ws_bytes);
   if (st != SPEC_OK) return st;
   if (!(std::isfinite(temperature) && temperature > 0.f)) return SPEC_ERR_ARG;
@@ -216,7 +217,7 @@ int run_verify(const void* target, const void* draft, int dtype, const int32_t* 
     p.emitted = emitted;
     p.n_acc = n_accepted;
     p.ws = specv::ws_carve(workspace, B, gamma, V);
-    return launch_status(specv::sample_launch(p, dtype, static_cast<cudaStream_t>(stream)));
+    return launch_status(specv::sample_launch(p, dtype, phases, static_cast<cudaStream_t>(stream)));
   }
 
   Plan plan;
@@ -263,6 +264,24 @@ int spec_verify_sample(const void* target_logits, const void* draft_logits, int 
   return run_verify(target_logits, draft_logits, dtype, draft_ids, draft_len, uniforms, temperature, B, gamma, V,
                     emitted, n_accepted, nullptr, nullptr, nullptr, nullptr, nullptr, workspace, ws_bytes, stream,
                     false);
+}
+
+int spec_verify_sample_stream(const void* target_logits, const void* draft_logits, int dtype,
+                              const int32_t* draft_ids, const int32_t* draft_len, const float* uniforms,
+                              float temperature, int B, int gamma, int V, int32_t* emitted, int32_t* n_accepted,
+                              void* workspace, size_t ws_bytes, void* stream) {
+  return run_verify(target_logits, draft_logits, dtype, draft_ids, draft_len, uniforms, temperature, B, gamma, V,
+                    emitted, n_accepted, nullptr, nullptr, nullptr, nullptr, nullptr, workspace, ws_bytes, stream,
+                    false, 1);
+}
+
+int spec_verify_sample_draw(const void* target_logits, const void* draft_logits, int dtype,
+                            const int32_t* draft_ids, const int32_t* draft_len, const float* uniforms,
+                            float temperature, int B, int gamma, int V, int32_t* emitted, int32_t* n_accepted,
+                            void* workspace, size_t ws_bytes, void* stream) {
+  return run_verify(target_logits, draft_logits, dtype, draft_ids, draft_len, uniforms, temperature, B, gamma, V,
+                    emitted, n_accepted, nullptr, nullptr, nullptr, nullptr, nullptr, workspace, ws_bytes, stream,
+                    false, 2);
 }
 
 int spec_accept_stats(const void* target_logits, const void* draft_logits, int dtype, const int32_t* draft_ids,

@@ -586,16 +586,16 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_draw_kernel(const Sa
   }
 }
 
-cudaError_t sample_launch(const SampleParams& p, int dtype, cudaStream_t stream) {
+cudaError_t sample_launch(const SampleParams& p, int dtype, int phases, cudaStream_t stream) {
   const dim3 block(kStreamThreads);
   const dim3 g1(static_cast<unsigned>((long long)p.B * (p.G + 1) * p.nslices));
   const dim3 g2(static_cast<unsigned>((long long)p.B * p.nslices));
   if (dtype == 0) {
-    verify_stream_kernel<float><<<g1, block, 0, stream>>>(p);
-    verify_draw_kernel<float><<<g2, block, 0, stream>>>(p);
+    if (phases & 1) verify_stream_kernel<float><<<g1, block, 0, stream>>>(p);
+    if (phases & 2) verify_draw_kernel<float><<<g2, block, 0, stream>>>(p);
   } else {
-    verify_stream_kernel<__nv_bfloat16><<<g1, block, 0, stream>>>(p);
-    verify_draw_kernel<__nv_bfloat16><<<g2, block, 0, stream>>>(p);
+    if (phases & 1) verify_stream_kernel<__nv_bfloat16><<<g1, block, 0, stream>>>(p);
+    if (phases & 2) verify_draw_kernel<__nv_bfloat16><<<g2, block, 0, stream>>>(p);
   }
   return cudaGetLastError();
 }

@@ -150,3 +150,18 @@ def test_cluster_sizes_agree(S, monkeypatch):
         assert max(worst.values()) <= 1.0, (cs, worst)
         outs.append(em.cpu())
     assert S.check_status() == 0
+
+
+@pytest.mark.parametrize("k", [1, 4])
+def test_split_phases_equal_the_whole_call(S, k):
+    """spec_verify_sample_stream then spec_verify_sample_draw is exactly spec_verify_sample."""
+    w = W.make(k, device="cuda", B=64 if k == 4 else None)
+    em, na = S.verify_sample(w.target, w.draft, w.ids, w.uniforms, w.T, w.draft_len)
+    em2 = torch.full_like(em, 7)
+    na2 = torch.full_like(na, 7)
+    S.verify_sample(w.target, w.draft, w.ids, w.uniforms, w.T, w.draft_len, emitted=em2, n_accepted=na2,
+                    phase="stream")
+    S.verify_sample(w.target, w.draft, w.ids, w.uniforms, w.T, w.draft_len, emitted=em2, n_accepted=na2,
+                    phase="draw")
+    assert S.check_status() == 0
+    assert torch.equal(em, em2) and torch.equal(na, na2)
