@@ -121,6 +121,32 @@ int spec_verify_sample_draw(const void* target_logits, const void* draft_logits,
                             int32_t* emitted, int32_t* n_accepted,
                             void* workspace, size_t ws_bytes, void* stream);
 
+/* spec_verify_sample without a workspace argument, for callers that cannot
+ * allocate device memory: for instance a plugin handed only its input and
+ * output buffers by a host program that owns every allocator, or a serving loop
+ * that must not call cudaMalloc once it is running (cudaMalloc can block on the
+ * whole device and can fail under memory pressure).  The paper has no
+ * counterpart to this entry point; it only changes where the scratch lives.
+ *
+ * The scratch is one fixed array of SPEC_NOALLOC_SCRATCH_BYTES inside this
+ * library, held by every GPU that loads the library until the process exits.
+ * Calls whose spec_workspace_size(B, gamma, V, dtype) exceeds it return
+ * SPEC_ERR_WORKSPACE without touching the GPU (use spec_verify_sample with a
+ * workspace of your own then).  The first call on a device looks up the
+ * array's device address on that device (cudaGetSymbolAddress); make that first
+ * call before any stream capture.  Every call uses the same array, so calls
+ * that overlap on the GPU (other streams, other threads) race and corrupt each
+ * other's results: serialise them.  Each call clears the counters it needs at
+ * zero on `stream` before its kernels (cudaMemsetAsync; nothing is allocated).
+ * Device-side findings are reported through n_accepted[b] = -1 and
+ * emitted[b, :] = -1 only, since the caller has no workspace to read an error
+ * word from.  Arguments, layouts and results otherwise as spec_verify_sample. */
+#define SPEC_NOALLOC_SCRATCH_BYTES (16u << 20)
+int spec_verify_sample_noalloc(const void* target_logits, const void* draft_logits, int dtype,
+                               const int32_t* draft_ids, const int32_t* draft_len, const float* uniforms,
+                               float temperature, int B, int gamma, int V,
+                               int32_t* emitted, int32_t* n_accepted, void* stream);
+
 /* Greedy verification: argmax standardisation (paper-graph-ui teardown §2.2;
  * multigrid.ai on sampling temperature).  a_i = argmax_k target[b,i,k], lowest
  * index on ties; guesses are accepted while a_i == draft_ids[b,i]; the emitted
