@@ -59,13 +59,14 @@ typedef enum {
   SPEC_ERR_WORKSPACE = 7     /* workspace too small or not 256-byte aligned */
 } spec_status_t;
 
-/* Bytes of device workspace the three entry points need for (B, gamma): an
- * error word, a per-row arrival counter and per-position records.  The
- * workspace must be zero-filled once before its first use (cudaMemset or
- * spec_workspace_init); every call leaves the counters and records it used at
- * zero again, so one workspace serves any sequence of calls on one stream.
- * Calls that overlap on the GPU must use different workspaces.  Returns 0 for
- * invalid sizes.  No CUDA call is made. */
+/* Bytes of device workspace the entry points need for (B, gamma, V): an error
+ * word, per-row arrival counters, greedy argmax keys, per-slice softmax
+ * normalisers, the logits at the draft tokens, and the slice and chunk masses
+ * of the drawn rows.  The workspace must be zero-filled once before its first
+ * use (cudaMemset or spec_workspace_init); every call leaves the slots it used
+ * at zero again, so one workspace serves any sequence of calls of any shape on
+ * one stream.  Calls that overlap on the GPU must use different workspaces.
+ * Returns 0 for invalid sizes.  No CUDA call is made. */
 size_t spec_workspace_size(int B, int gamma, int V, int dtype);
 
 /* Zero-fills `ws_bytes` of workspace on `stream` (cudaMemsetAsync). */
