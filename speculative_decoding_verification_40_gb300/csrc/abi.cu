@@ -158,6 +158,45 @@ int resolve_plan(int V, int dtype, Plan* out) {
   return SPEC_OK;
 }
 
+// Streaming multiprocessors of the current device (cached per device), 0 if the query fails.
+int device_sms() {
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return 0;
+  }
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    cache[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
+// Vocabulary elements per draw CTA.  A draw CTA re-reads its slice of one row only if that row
+// draws there, so wide slices cost little traffic; they are halved (32768 -> 16384) only when the
+// batch would otherwise give fewer than three draw CTAs per SM.  At least V/32 (at most 32 draw CTAs
+// per row), a multiple of the draw chunk; SPECVERIFY_DSLICE (elements) overrides within the limits.
+int draw_slice(int B, int V, int dtype) {
+  const int chunk = 4 * 32 * (dtype == SPEC_F32 ? 4 : 8);
+  const long long wide = 32768;
+  const long long ctas = static_cast<long long>(B) * ((V + wide - 1) / wide);
+  int slice = ctas >= 3LL * device_sms() ? 32768 : 16384;
+  if (const char* env = std::getenv("SPECVERIFY_DSLICE")) {
+    const int want = std::atoi(env);
+    if (want > 0) slice = want;
+  }
+  const int lo = (V + specv::kMaxSlices - 1) / specv::kMaxSlices;
+  if (slice < lo) slice = lo;
+  slice = static_cast<int>(align_up(slice, chunk));
+  if (slice > specv::kMaxChunksPerSlice * chunk) slice = specv::kMaxChunksPerSlice * chunk;
+  return slice;
+}
+
 bool rows_aligned(const void* p, int V, int esz) {
   return (reinterpret_cast<uintptr_t>(p) % 16 == 0) && ((static_cast<size_t>(V) * esz) % 16 == 0);
 }
@@ -213,6 +252,8 @@ int run_verify(const void* target, const void* draft, int dtype, const int32_t* 
     p.V = V;
     p.slice = sample_slice(V, dtype);
     p.nslices = (V + p.slice - 1) / p.slice;
+    p.dslice = draw_slice(B, V, dtype);
+    p.ndslices = (V + p.dslice - 1) / p.dslice;
     p.vec = vec ? 1 : 0;
     p.emitted = emitted;
     p.n_acc = n_accepted;

@@ -47,7 +47,9 @@ struct SampleParams {
   float scale;               // log2(e) / T
   int B, G, V;
   int slice;                 // vocabulary elements per work item (a multiple of 32 x elements per 16 bytes)
-  int nslices;               // work items per logit row (<= kMaxSlices)
+  int nslices;               // stream CTAs per logit row (<= kMaxSlices)
+  int dslice;                // vocabulary elements per draw CTA (a multiple of the draw chunk)
+  int ndslices;              // draw CTAs per batch row (<= kMaxSlices)
   int vec;                   // every logit row starts on a 16-byte boundary
   int32_t* emitted;          // [B, G+1]
   int32_t* n_acc;            // [B]

@@ -83,6 +83,69 @@ __device__ __forceinline__ void merge(float& m, float& s, float om, float os, fl
   m = M;
 }
 
+// NaN-propagating max of U 16-byte vectors of raw logits, as float32.
+template <typename T, int U>
+struct GroupMax;
+
+template <int U>
+struct GroupMax<float, U> {
+  __device__ static __forceinline__ float get(const uint4 (&r)[U]) {
+    float m = __uint_as_float(r[0].x);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      m = max_nan(m, __uint_as_float(r[u].x));
+      m = max_nan(m, __uint_as_float(r[u].y));
+      m = max_nan(m, __uint_as_float(r[u].z));
+      m = max_nan(m, __uint_as_float(r[u].w));
+    }
+    return m;
+  }
+};
+
+template <int U>
+struct GroupMax<__nv_bfloat16, U> {
+  // pairs of bf16 compared two at a time on the packed words, then the last pair widened
+  __device__ static __forceinline__ uint32_t max2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+  }
+  __device__ static __forceinline__ float get(const uint4 (&r)[U]) {
+    uint32_t m = max2(max2(r[0].x, r[0].y), max2(r[0].z, r[0].w));
+#pragma unroll
+    for (int u = 1; u < U; ++u) m = max2(m, max2(max2(r[u].x, r[u].y), max2(r[u].z, r[u].w)));
+    return max_nan(__uint_as_float(m << 16), __uint_as_float(m & 0xffff0000u));
+  }
+};
+
+// Online normaliser update with U 16-byte vectors of raw logits: one max and one rescale per group,
+// then 2^((l - m) log2(e)/T) per element as a single FFMA and a hardware exp2.
+template <typename T, int U>
+__device__ __forceinline__ void online_group(float& m, float& s, float& raw, const uint4 (&r)[U], float sc) {
+  constexpr int kV = Elems<T>::kVec;
+  const float vm = GroupMax<T, U>::get(r);
+  raw = max_nan(raw, vm);
+  if (vm > -INFINITY) {
+    if (vm > m) {
+      s *= fast_exp2((m - vm) * sc);
+      m = vm;
+    }
+    const float nc = -m * sc;
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float f[kV];
+      Elems<T>::widen(r[u], f);
+#pragma unroll
+      for (int j = 0; j < kV; j += 2) {
+        a0 += fast_exp2(fmaf(f[j], sc, nc));
+        a1 += fast_exp2(fmaf(f[j + 1], sc, nc));
+      }
+    }
+    s += a0 + a1;
+  }
+}
+
 // Weights of one lane's kV elements starting at `base` of the drawn row(s): p, and w = max(0, p - q)
 // for a residual draw (w = p otherwise); elements past V weigh 0.  The mass pass and the final scan
 // both use this arithmetic, so they see identical weights.
@@ -215,10 +278,10 @@ __device__ void resolve_row(const SampleParams& a, int b, int gb, const RowState
   constexpr int kV = Elems<T>::kVec;
   const int tid = threadIdx.x, lane = tid & 31;
   const int G1 = a.G + 1;
-  const int ND = a.nslices;
+  const int ND = a.ndslices;
   const int seg = 32 * kV;
   const int cpc = kR * seg;
-  const int cps = a.slice / cpc;
+  const int cps = a.dslice / cpc;
   const int nc = (a.V + cpc - 1) / cpc;
   float2* dsum = reinterpret_cast<float2*>(a.ws.dsum) + (size_t)b * ND;
   float2* dch = reinterpret_cast<float2*>(a.ws.dch) + (size_t)b * ND * cps;
@@ -381,6 +444,8 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_stream_kernel(const 
   constexpr int kV = Elems<T>::kVec;
   constexpr int U = 4;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // the draw kernel may be scheduled once every stream CTA is running; it waits for their results
+  asm volatile("griddepcontrol.launch_dependents;");
   const int NS = a.nslices;
   const int s = blockIdx.x % NS;
   const int pos = blockIdx.x / NS;
@@ -411,38 +476,25 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_stream_kernel(const 
         for (int u = 0; u < U; ++u) r0[u] = ldg_stream(t4 + v + u * kST);
 #pragma unroll
         for (int u = 0; u < U; ++u) r1[u] = ldg_stream(d4 + v + u * kST);
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          float f[kV];
-          Elems<T>::widen(r0[u], f);
-          online<kV>(mp, sp, rp, f, sc);
-          Elems<T>::widen(r1[u], f);
-          online<kV>(mq, sq, rq, f, sc);
-        }
+        online_group<T, U>(mp, sp, rp, r0, sc);
+        online_group<T, U>(mq, sq, rq, r1, sc);
       }
       for (; v < nv; v += kST) {
-        float f[kV];
-        Elems<T>::widen(ldg_stream(t4 + v), f);
-        online<kV>(mp, sp, rp, f, sc);
-        Elems<T>::widen(ldg_stream(d4 + v), f);
-        online<kV>(mq, sq, rq, f, sc);
+        const uint4 r0[1] = {ldg_stream(t4 + v)};
+        const uint4 r1[1] = {ldg_stream(d4 + v)};
+        online_group<T, 1>(mp, sp, rp, r0, sc);
+        online_group<T, 1>(mq, sq, rq, r1, sc);
       }
     } else {
       for (; v + (U - 1) * kST < nv; v += U * kST) {
         uint4 r0[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) r0[u] = ldg_stream(t4 + v + u * kST);
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          float f[kV];
-          Elems<T>::widen(r0[u], f);
-          online<kV>(mp, sp, rp, f, sc);
-        }
+        online_group<T, U>(mp, sp, rp, r0, sc);
       }
       for (; v < nv; v += kST) {
-        float f[kV];
-        Elems<T>::widen(ldg_stream(t4 + v), f);
-        online<kV>(mp, sp, rp, f, sc);
+        const uint4 r0[1] = {ldg_stream(t4 + v)};
+        online_group<T, 1>(mp, sp, rp, r0, sc);
       }
     }
     done = nv * kV;
@@ -498,11 +550,13 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_draw_kernel(const Sa
   __shared__ DrawSmem sm;
   constexpr int kV = Elems<T>::kVec;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int ND = a.nslices;
+  const int ND = a.ndslices;
   const int b = a.B - 1 - static_cast<int>(blockIdx.x / ND);  // last-streamed rows first: still in L2
   const int d = static_cast<int>(blockIdx.x % ND);
   const int G1 = a.G + 1;
   const int gb = a.draft_len ? __ldg(a.draft_len + b) : a.G;
+  // launched as a programmatic dependent of the stream kernel: wait for all of it (and its writes)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (gb < 0 || gb > a.G) {  // invalid draft length: nothing was streamed for this row
     if (d == 0 && tid == 0) {
       int32_t* e = a.emitted + (size_t)b * G1;
@@ -520,7 +574,7 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_draw_kernel(const Sa
     const T* dr = resid ? reinterpret_cast<const T*>(a.draft) + ((size_t)b * a.G + st.n) * a.V : tr;
     const int seg = 32 * kV;                     // elements per segment
     const int cpc = kR * seg;                    // elements per chunk
-    const int cps = a.slice / cpc;               // chunks per slice
+    const int cps = a.dslice / cpc;              // chunks per slice
     const int c0 = d * cps;
     const int c1 = min(c0 + cps, (a.V + cpc - 1) / cpc);
     const float sc = a.scale;
@@ -586,18 +640,34 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_draw_kernel(const Sa
   }
 }
 
+template <typename T>
+static cudaError_t launch_draw(const SampleParams& p, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((long long)p.B * p.ndslices));
+  cfg.blockDim = dim3(kStreamThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, verify_draw_kernel<T>, p);
+}
+
 cudaError_t sample_launch(const SampleParams& p, int dtype, int phases, cudaStream_t stream) {
   const dim3 block(kStreamThreads);
   const dim3 g1(static_cast<unsigned>((long long)p.B * (p.G + 1) * p.nslices));
-  const dim3 g2(static_cast<unsigned>((long long)p.B * p.nslices));
+  cudaError_t e = cudaSuccess;
   if (dtype == 0) {
     if (phases & 1) verify_stream_kernel<float><<<g1, block, 0, stream>>>(p);
-    if (phases & 2) verify_draw_kernel<float><<<g2, block, 0, stream>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (phases & 2) e = launch_draw<float>(p, stream);
   } else {
     if (phases & 1) verify_stream_kernel<__nv_bfloat16><<<g1, block, 0, stream>>>(p);
-    if (phases & 2) verify_draw_kernel<__nv_bfloat16><<<g2, block, 0, stream>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (phases & 2) e = launch_draw<__nv_bfloat16>(p, stream);
   }
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace specv
