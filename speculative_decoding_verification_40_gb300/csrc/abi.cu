@@ -14,57 +14,45 @@ namespace {
 
 using specv::align_up;
 
-constexpr int kSmemPreferred = 100 * 1024;  // leaves room for two CTAs per SM
-constexpr int kSmemMax = 227 * 1024 - 2048; // opt-in limit minus the kernel's static shared memory
+constexpr int kStatsSliceBytes = 64 * 1024;  // bytes of each row a statistics CTA streams
 constexpr int kMaxDevices = 64;
 
 struct Plan {
   int cs;     // CTAs per cluster (vocabulary slices per row)
   int L;      // slice length in elements
   int smem;   // dynamic shared memory per CTA
+  int nclus;  // clusters the device holds at once (0 until checked on a device)
 };
 
-int smem_for(int L) {
-  const int Lpad = static_cast<int>(align_up(L, specv::kChunk));
-  return 2 * Lpad * 4;
-}
-
-Plan plan_for(int V, int cs) {
+// Statistics kernel: CS CTAs per position, each streaming about 32 KB of each row (at most 16,
+// the largest cluster); no dynamic shared memory.
+Plan plan_for(int V, int cs, int dtype) {
+  (void)dtype;
   Plan p;
   p.cs = cs;
   p.L = static_cast<int>(align_up((V + cs - 1) / cs, 8));
-  p.smem = smem_for(p.L);
+  p.smem = 0;
+  p.nclus = 0;
   return p;
 }
 
-// Smallest cluster whose slice fits the preferred shared-memory budget; an
-// explicit SPECVERIFY_CLUSTER (1, 2, 4, 8 or 16) overrides the choice.
-bool choose_plan(int V, Plan* out) {
+// SPECVERIFY_CLUSTER (1 to 16) overrides the cluster size.
+bool choose_plan(int V, int dtype, Plan* out) {
+  const long long esz = dtype == SPEC_F32 ? 4 : 2;
+  long long slice = kStatsSliceBytes;
+  if (const char* env = std::getenv("SPECVERIFY_STATS_SLICE")) {
+    const long long want = std::atoll(env);
+    if (want > 0) slice = want;
+  }
+  long long cs = (static_cast<long long>(V) * esz + slice - 1) / slice;
+  if (cs < 1) cs = 1;
+  if (cs > specv::kMaxCluster) cs = specv::kMaxCluster;
   if (const char* env = std::getenv("SPECVERIFY_CLUSTER")) {
-    const int cs = std::atoi(env);
-    if (cs == 1 || cs == 2 || cs == 4 || cs == 8 || cs == 16) {
-      Plan p = plan_for(V, cs);
-      if (p.smem <= kSmemMax) {
-        *out = p;
-        return true;
-      }
-    }
+    const int want = std::atoi(env);
+    if (want >= 1 && want <= specv::kMaxCluster) cs = want;
   }
-  for (int cs = 1; cs <= specv::kMaxCluster; cs *= 2) {
-    Plan p = plan_for(V, cs);
-    if (p.smem <= kSmemPreferred) {
-      *out = p;
-      return true;
-    }
-  }
-  for (int cs = 1; cs <= specv::kMaxCluster; cs *= 2) {
-    Plan p = plan_for(V, cs);
-    if (p.smem <= kSmemMax) {
-      *out = p;
-      return true;
-    }
-  }
-  return false;
+  *out = plan_for(V, static_cast<int>(cs), dtype);
+  return true;
 }
 
 // Kernel attributes are per device; set them once per (device, kernel, dtype).
@@ -78,7 +66,7 @@ int prepare(int dtype) {
   if (flag.load(std::memory_order_acquire)) return SPEC_OK;
   std::lock_guard<std::mutex> lk(g_prep_mu);
   if (!flag.load(std::memory_order_relaxed)) {
-    if (specv::stats_prepare(dtype, kSmemMax) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (specv::stats_prepare(dtype) != cudaSuccess) return SPEC_ERR_CUDA;
     flag.store(1, std::memory_order_release);
   }
   return SPEC_OK;
@@ -105,15 +93,16 @@ int sample_slice(int V, int dtype) {
 int schedulable_plan(int V, int dtype, Plan* plan) {
   for (int tries = 0; tries < 5; ++tries) {
     int n = 0;
-    if (specv::stats_max_active_clusters(dtype, plan->cs, plan->smem, &n) != cudaSuccess) {
+    if (specv::stats_max_active_clusters(dtype, plan->cs, &n) != cudaSuccess) {
       cudaGetLastError();
       return SPEC_ERR_CUDA;
     }
-    if (n > 0) return SPEC_OK;
+    if (n > 0) {
+      plan->nclus = n;
+      return SPEC_OK;
+    }
     if (plan->cs == 1) return SPEC_ERR_ARG;
-    Plan q = plan_for(V, plan->cs / 2);
-    if (q.smem > kSmemMax) return SPEC_ERR_ARG;
-    *plan = q;
+    *plan = plan_for(V, plan->cs / 2, dtype);
   }
   return SPEC_ERR_ARG;
 }
@@ -148,7 +137,7 @@ int resolve_plan(int V, int dtype, Plan* out) {
     }
   }
   Plan plan;
-  if (!choose_plan(V, &plan)) return SPEC_ERR_ARG;
+  if (!choose_plan(V, dtype, &plan)) return SPEC_ERR_ARG;
   int st = prepare(dtype);
   if (st != SPEC_OK) return st;
   if ((st = schedulable_plan(V, dtype, &plan)) != SPEC_OK) return st;
@@ -281,7 +270,7 @@ int run_verify(const void* target, const void* draft, int dtype, const int32_t* 
   p.accept_prob = accept_prob;
   p.resid = resid;
   p.ws = specv::ws_carve(workspace, B, gamma, V);
-  return launch_status(specv::stats_launch(p, dtype, plan.cs, plan.smem, static_cast<cudaStream_t>(stream)));
+  return launch_status(specv::stats_launch(p, dtype, plan.cs, static_cast<cudaStream_t>(stream)));
 }
 
 }  // namespace
@@ -389,7 +378,7 @@ int spec_verify_plan(int B, int gamma, int V, int dtype, int* cluster_size, int*
     if ((st = resolve_plan(V, dtype, &plan)) != SPEC_OK) return st;
   } else {
     cudaGetLastError();  // no device: report the plan before the co-scheduling check
-    if (!choose_plan(V, &plan)) return SPEC_ERR_ARG;
+    if (!choose_plan(V, dtype, &plan)) return SPEC_ERR_ARG;
   }
   if (cluster_size) *cluster_size = plan.cs;
   if (slice_len) *slice_len = plan.L;

@@ -8,9 +8,7 @@
 namespace specv {
 
 // ---------------------------------------------------------------- launch constants
-constexpr int kThreads = 512;          // threads per CTA of the sampling / statistics kernel
-constexpr int kWarps = kThreads / 32;
-constexpr int kChunk = 128;            // elements per warp-chunk: 32 lanes x 4 consecutive elements
+constexpr int kStatsThreads = 256;     // threads per CTA of the statistics kernel
 constexpr int kMaxCluster = 16;        // largest thread-block cluster (non-portable size)
 constexpr int kGreedyThreads = 256;    // threads per CTA of the greedy kernel
 constexpr int kGreedySlice = 8192;     // target-row elements per greedy CTA
@@ -121,6 +119,47 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
       : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
       : "l"(p));
   return r;
+}
+
+// mbarrier and bulk-copy (TMA) helpers.  Every wait is bounded: it gives up after `limit` polls.
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Makes mbarrier initialisations visible to the asynchronous (bulk-copy) proxy.
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// Global -> this CTA's shared memory, `bytes` (a multiple of 16, both addresses 16-byte aligned),
+// completing on mbarrier `bar`.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+// Orders this thread's earlier shared-memory accesses before later bulk-copy (async proxy) accesses.
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Waits for the barrier's phase with the given parity to complete; false if it did not within `limit` polls.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit) {
+  for (uint32_t it = 0; it < limit; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
 }
 
 // max that propagates NaN: a NaN anywhere in a row survives the reduction.

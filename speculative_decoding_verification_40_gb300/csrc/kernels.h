@@ -57,9 +57,9 @@ struct SampleParams {
 };
 
 // dtype: 0 = float32, 1 = bfloat16.  stats selects the statistics kernel.
-cudaError_t stats_prepare(int dtype, int smem);
-cudaError_t stats_max_active_clusters(int dtype, int cs, int smem, int* out);
-cudaError_t stats_launch(const VerifyParams& p, int dtype, int cs, int smem, cudaStream_t stream);
+cudaError_t stats_prepare(int dtype);
+cudaError_t stats_max_active_clusters(int dtype, int cs, int* out);
+cudaError_t stats_launch(const VerifyParams& p, int dtype, int cs, cudaStream_t stream);
 // phases: 1 = stream kernel, 2 = draw kernel, 3 = both
 cudaError_t sample_launch(const SampleParams& p, int dtype, int phases, cudaStream_t stream);
 cudaError_t greedy_launch(const GreedyParams& p, int dtype, cudaStream_t stream);

@@ -31,6 +31,7 @@
 // plus at most the two drawn rows per batch row that have left L2.
 #include "common.cuh"
 #include "kernels.h"
+#include "softmax.cuh"
 
 namespace specv {
 
@@ -47,104 +48,6 @@ struct RowState {
   uint32_t err;
   float mp, ip, mq, iq;
 };
-
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// Online normaliser update with a group of raw logits.
-template <int kCnt>
-__device__ __forceinline__ void online(float& m, float& s, float& raw, const float* f, float sc) {
-  float vm = f[0];
-#pragma unroll
-  for (int j = 1; j < kCnt; ++j) vm = max_nan(vm, f[j]);
-  raw = max_nan(raw, vm);
-  if (vm > -INFINITY) {
-    if (vm > m) {
-      s *= fast_exp2((m - vm) * sc);
-      m = vm;
-    }
-    float acc = 0.f;
-#pragma unroll
-    for (int j = 0; j < kCnt; ++j) acc += fast_exp2((f[j] - m) * sc);
-    s += acc;
-  }
-}
-
-// Merge normaliser (om, os) into (m, s).
-__device__ __forceinline__ void merge(float& m, float& s, float om, float os, float sc) {
-  const float M = fmaxf(m, om);
-  if (!(M > -INFINITY)) return;  // both empty
-  const float x = m > -INFINITY ? s * fast_exp2((m - M) * sc) : 0.f;
-  const float y = om > -INFINITY ? os * fast_exp2((om - M) * sc) : 0.f;
-  s = x + y;
-  m = M;
-}
-
-// NaN-propagating max of U 16-byte vectors of raw logits, as float32.
-template <typename T, int U>
-struct GroupMax;
-
-template <int U>
-struct GroupMax<float, U> {
-  __device__ static __forceinline__ float get(const uint4 (&r)[U]) {
-    float m = __uint_as_float(r[0].x);
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      m = max_nan(m, __uint_as_float(r[u].x));
-      m = max_nan(m, __uint_as_float(r[u].y));
-      m = max_nan(m, __uint_as_float(r[u].z));
-      m = max_nan(m, __uint_as_float(r[u].w));
-    }
-    return m;
-  }
-};
-
-template <int U>
-struct GroupMax<__nv_bfloat16, U> {
-  // pairs of bf16 compared two at a time on the packed words, then the last pair widened
-  __device__ static __forceinline__ uint32_t max2(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-  }
-  __device__ static __forceinline__ float get(const uint4 (&r)[U]) {
-    uint32_t m = max2(max2(r[0].x, r[0].y), max2(r[0].z, r[0].w));
-#pragma unroll
-    for (int u = 1; u < U; ++u) m = max2(m, max2(max2(r[u].x, r[u].y), max2(r[u].z, r[u].w)));
-    return max_nan(__uint_as_float(m << 16), __uint_as_float(m & 0xffff0000u));
-  }
-};
-
-// Online normaliser update with U 16-byte vectors of raw logits: one max and one rescale per group,
-// then 2^((l - m) log2(e)/T) per element as a single FFMA and a hardware exp2.
-template <typename T, int U>
-__device__ __forceinline__ void online_group(float& m, float& s, float& raw, const uint4 (&r)[U], float sc) {
-  constexpr int kV = Elems<T>::kVec;
-  const float vm = GroupMax<T, U>::get(r);
-  raw = max_nan(raw, vm);
-  if (vm > -INFINITY) {
-    if (vm > m) {
-      s *= fast_exp2((m - vm) * sc);
-      m = vm;
-    }
-    const float nc = -m * sc;
-    float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      float f[kV];
-      Elems<T>::widen(r[u], f);
-#pragma unroll
-      for (int j = 0; j < kV; j += 2) {
-        a0 += fast_exp2(fmaf(f[j], sc, nc));
-        a1 += fast_exp2(fmaf(f[j + 1], sc, nc));
-      }
-    }
-    s += a0 + a1;
-  }
-}
 
 // Weights of one lane's kV elements starting at `base` of the drawn row(s): p, and w = max(0, p - q)
 // for a residual draw (w = p otherwise); elements past V weigh 0.  The mass pass and the final scan

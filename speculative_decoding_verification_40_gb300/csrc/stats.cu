@@ -7,166 +7,50 @@
 // and p(x_i), q(x_i), min(1, p(x_i)/q(x_i)) at the draft token, with p and q
 // the temperature softmaxes of the target and draft rows (§2.2).
 //
-// Work decomposition.  One thread-block cluster of CS CTAs per (batch row b,
-// position i); CTA r of the cluster owns the vocabulary slice [r*L, r*L + L)
-// of target and draft row (b, i).  Each CTA
-//   1. streams its slices from HBM into shared memory as float32 (16-byte
-//      loads, no L1 allocation) and takes the slice max;
-//   2. replaces each logit by 2^((l - m_slice) * log2(e)/T) and sums them;
-//   3. exchanges (max, sum) with the other CTAs through distributed shared
-//      memory, so every CTA holds the row normalisers and its own scale
-//      a_r = 2^((m_slice - m_row) log2(e)/T) / S_row (p = e * a_r);
-//   4. sums min(p, q) and max(0, p - q) over its slice;
-//   5. exchanges those sums; the CTA owning x_i supplies p(x_i), q(x_i), and
-//      rank 0 writes the position's statistics.
-// Every logit is read from HBM once; p and q never leave shared memory.
+// beta needs the row normalisers of p and q before any element can be
+// compared.  One thread-block cluster of CS CTAs per (batch row b, position
+// i); CTA r of the cluster owns the vocabulary slice [r*L, r*L + L) of target
+// and draft row (b, i).  Each CTA
+//   1. streams its two slices from HBM (16-byte loads, no L1 allocation),
+//      keeping online softmax normalisers (running max m,
+//      S = sum 2^((l - m) log2(e)/T)) for p and q;
+//   2. pushes its (m, S) pair into every CTA of the cluster (distributed
+//      shared memory stores) and meets them at a cluster barrier, so every CTA
+//      combines the same values in the same order;
+//   3. reads its slices again -- microseconds later, from L2 -- with
+//      p = 2^(l log2(e)/T - c_p), c_p = m log2(e)/T + log2 S (likewise q),
+//      summing min(p, q) and p; the residual mass is
+//      sum p - sum min(p, q) = sum max(0, p - q);
+//   4. pushes those sums, and p(x_i), q(x_i) if it owns x_i, to rank 0, which
+//      writes the position's statistics after a second cluster barrier.
+// HBM traffic is the logits once (the second read hits L2: the slices a whole
+// GPU of resident CTAs holds between the two reads are a few tens of MB); no
+// CTA touches another's shared memory after the second barrier.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "softmax.cuh"
 
 namespace specv {
 
 namespace {
 
-struct Xch1 {  // per-CTA slice normalisers
-  float mp, sp, mq, sq;
-};
-struct Xch2 {  // per-CTA slice overlaps and the values at the draft token
-  float beta, z, psum, px, qx;
-};
+constexpr int kT = kStatsThreads;
+constexpr int kW = kT / 32;
+constexpr int kU = 4;  // 16-byte loads in flight per thread and row
+constexpr int kMinBlocks = 4;  // resident CTAs per SM the register budget is sized for
 
-// Copies n logits of one row (and of a second row when two_rows) to shared
-// memory as float32 and returns this thread's NaN-propagating maxima.  Entries
-// [n, fill_to) are set to -inf.
-template <typename T>
-__device__ __forceinline__ void load_rows(const T* __restrict__ src0, const T* __restrict__ src1, bool two_rows,
-                                          int n, int fill_to, bool vec, float* __restrict__ dst0,
-                                          float* __restrict__ dst1, float& m0, float& m1) {
-  constexpr int kV = Elems<T>::kVec;
-  constexpr int U = 4;
-  const int tid = threadIdx.x;
-  m0 = -INFINITY;
-  m1 = -INFINITY;
-  int done = 0;
-  if (vec) {
-    const int nv = n / kV;
-    const uint4* s0 = reinterpret_cast<const uint4*>(src0);
-    const uint4* s1 = reinterpret_cast<const uint4*>(src1);
-    int v = tid;
-    if (two_rows) {
-      for (; v + (U - 1) * kThreads < nv; v += U * kThreads) {
-        uint4 r0[U], r1[U];
+// Adds min(p, q) and p over kV elements of each row, p = 2^(l_p sc + ncp), q = 2^(l_q sc + ncq).
+template <int kV>
+__device__ __forceinline__ void overlap(const float* f, const float* g, float sc, float ncp, float ncq, float& tmin,
+                                        float& tp) {
 #pragma unroll
-        for (int u = 0; u < U; ++u) r0[u] = ldg_stream(s0 + v + u * kThreads);
-#pragma unroll
-        for (int u = 0; u < U; ++u) r1[u] = ldg_stream(s1 + v + u * kThreads);
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          float f[kV], g[kV];
-          Elems<T>::widen(r0[u], f);
-          Elems<T>::widen(r1[u], g);
-#pragma unroll
-          for (int j = 0; j < kV; ++j) {
-            m0 = max_nan(m0, f[j]);
-            m1 = max_nan(m1, g[j]);
-          }
-          store_f32<kV>(dst0 + (v + u * kThreads) * kV, f);
-          store_f32<kV>(dst1 + (v + u * kThreads) * kV, g);
-        }
-      }
-      for (; v < nv; v += kThreads) {
-        const uint4 r0 = ldg_stream(s0 + v);
-        const uint4 r1 = ldg_stream(s1 + v);
-        float f[kV], g[kV];
-        Elems<T>::widen(r0, f);
-        Elems<T>::widen(r1, g);
-#pragma unroll
-        for (int j = 0; j < kV; ++j) {
-          m0 = max_nan(m0, f[j]);
-          m1 = max_nan(m1, g[j]);
-        }
-        store_f32<kV>(dst0 + v * kV, f);
-        store_f32<kV>(dst1 + v * kV, g);
-      }
-    } else {
-      for (; v + (U - 1) * kThreads < nv; v += U * kThreads) {
-        uint4 r0[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) r0[u] = ldg_stream(s0 + v + u * kThreads);
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          float f[kV];
-          Elems<T>::widen(r0[u], f);
-#pragma unroll
-          for (int j = 0; j < kV; ++j) m0 = max_nan(m0, f[j]);
-          store_f32<kV>(dst0 + (v + u * kThreads) * kV, f);
-        }
-      }
-      for (; v < nv; v += kThreads) {
-        const uint4 r0 = ldg_stream(s0 + v);
-        float f[kV];
-        Elems<T>::widen(r0, f);
-#pragma unroll
-        for (int j = 0; j < kV; ++j) m0 = max_nan(m0, f[j]);
-        store_f32<kV>(dst0 + v * kV, f);
-      }
-    }
-    done = nv * kV;
-  }
-  for (int k = done + tid; k < n; k += kThreads) {
-    const float f = Elems<T>::one(src0, k);
-    m0 = max_nan(m0, f);
-    dst0[k] = f;
-    if (two_rows) {
-      const float g = Elems<T>::one(src1, k);
-      m1 = max_nan(m1, g);
-      dst1[k] = g;
-    }
-  }
-  for (int k = n + tid; k < fill_to; k += kThreads) {
-    dst0[k] = -INFINITY;
-    if (two_rows) dst1[k] = -INFINITY;
-  }
-}
-
-// In-place e = 2^((l - m) * sc) over [0, len) (len a multiple of 4); returns this thread's sum.
-__device__ __forceinline__ float exp_rows(float* __restrict__ s, int len, float m, float sc) {
-  float acc = 0.f;
-  if (!(m > -INFINITY) || !(m < INFINITY)) {  // empty / all -inf slice, or an invalid row
-    for (int k = threadIdx.x * 4; k < len; k += kThreads * 4)
-      *reinterpret_cast<float4*>(s + k) = make_float4(0.f, 0.f, 0.f, 0.f);
-    return 0.f;
-  }
-  for (int k = threadIdx.x * 4; k < len; k += kThreads * 4) {
-    float4 v = *reinterpret_cast<const float4*>(s + k);
-    v.x = exp2f((v.x - m) * sc);
-    v.y = exp2f((v.y - m) * sc);
-    v.z = exp2f((v.z - m) * sc);
-    v.w = exp2f((v.w - m) * sc);
-    acc += (v.x + v.y) + (v.z + v.w);
-    *reinterpret_cast<float4*>(s + k) = v;
-  }
-  return acc;
-}
-
-// Block reduction of N values (sum, or NaN-propagating max); every thread gets
-// the result, combined in a fixed order so all CTAs agree bit for bit.
-template <int N, bool kMax>
-__device__ __forceinline__ void block_reduce(float (&v)[N], float* red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int j = 0; j < N; ++j) v[j] = kMax ? warp_max_nan(v[j]) : warp_sum(v[j]);
-  if (lane == 0) {
-#pragma unroll
-    for (int j = 0; j < N; ++j) red[warp * N + j] = v[j];
-  }
-  __syncthreads();
-#pragma unroll
-  for (int j = 0; j < N; ++j) {
-    float a = red[j];
-    for (int w = 1; w < kWarps; ++w) a = kMax ? max_nan(a, red[w * N + j]) : a + red[w * N + j];
-    v[j] = a;
+  for (int j = 0; j < kV; ++j) {
+    const float p = fast_exp2(fmaf(f[j], sc, ncp));
+    const float q = fast_exp2(fmaf(g[j], sc, ncq));
+    tmin += fminf(p, q);
+    tp += p;
   }
 }
 
@@ -179,17 +63,20 @@ __device__ __forceinline__ void write_stats(const VerifyParams& a, size_t o, flo
   if (a.resid) a.resid[o] = z;
 }
 
+__device__ __forceinline__ void dsmem_st_v4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
 }  // namespace
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 2) stats_rows_kernel(const VerifyParams a) {
-  extern __shared__ __align__(16) float smem[];
-  __shared__ Xch1 x1;
-  __shared__ Xch2 x2;
-  __shared__ float red0[kWarps * 2];
-  __shared__ float red1[kWarps * 2];
-  __shared__ float red2[kWarps * 2];
+__global__ void __launch_bounds__(kT, kMinBlocks) stats_rows_kernel(const VerifyParams a) {
+  __shared__ __align__(16) float x1[kMaxCluster][4];  // (m_p, S_p, m_q, S_q) of every CTA; NaN maxima if bad
+  __shared__ __align__(16) float x2[kMaxCluster][4];  // rank 0: sum min(p,q), sum max(0,p-q), p(x), q(x)
+  __shared__ float red[5][kW];
   __shared__ float bc[4];
+  constexpr int kV = Elems<T>::kVec;
 
   const int CS = static_cast<int>(cluster_nctarank());
   const int rank = static_cast<int>(cluster_ctarank());
@@ -198,106 +85,180 @@ __global__ void __launch_bounds__(kThreads, 2) stats_rows_kernel(const VerifyPar
   const int i = pos - b * a.G;
   const int G1 = a.G + 1;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const size_t o = (size_t)b * a.G + i;
 
   const int gb = a.draft_len ? __ldg(a.draft_len + b) : a.G;
   if (gb < 0 || gb > a.G || i >= gb) {  // the whole cluster leaves together; padded positions are never read
     if (rank == 0 && tid == 0) {
-      write_stats(a, o, NAN, NAN, NAN, NAN, NAN);
+      write_stats(a, pos, NAN, NAN, NAN, NAN, NAN);
       if (gb < 0 || gb > a.G) atomicOr(a.ws.err, kErrArg);
     }
     return;
   }
   const int lo = rank * a.L;
   const int n = max(0, min(a.V, lo + a.L) - lo);
-  const int nch = (n + kChunk - 1) / kChunk;
-  const int Lpad = static_cast<int>(align_up(a.L, kChunk));
-  float* sP = smem;
-  float* sQ = smem + Lpad;
   const float sc = a.scale;
   const T* tp = reinterpret_cast<const T*>(a.target) + ((size_t)b * G1 + i) * a.V + lo;
-  const T* dp = reinterpret_cast<const T*>(a.draft) + ((size_t)b * a.G + i) * a.V + lo;
+  const T* dp = reinterpret_cast<const T*>(a.draft) + (size_t)pos * a.V + lo;
+  const uint4* t4 = reinterpret_cast<const uint4*>(tp);
+  const uint4* d4 = reinterpret_cast<const uint4*>(dp);
+  const int nv = a.vec ? n / kV : 0;  // 16-byte vectors (rows on a 16-byte boundary); scalar tail after them
+  const int x = __ldg(a.ids + pos);
+  const bool owner = x >= lo && x < lo + n;
+  float lpx = 0.f, lqx = 0.f;  // logits at the draft token, loaded early by the thread that reports them
+  if (tid == 0 && owner) {
+    lpx = Elems<T>::one(tp, x - lo);
+    lqx = Elems<T>::one(dp, x - lo);
+  }
 
-  // 1. slices to shared memory, slice maxima
-  float m2[2];
-  load_rows<T>(tp, dp, true, n, nch * kChunk, a.vec != 0, sP, sQ, m2[0], m2[1]);
-  block_reduce<2, true>(m2, red0);
-  const float Mp = m2[0], Mq = m2[1];
+  // 1. online normalisers of the slices, streamed from HBM
+  float mp = -INFINITY, sp = 0.f, rp = -INFINITY;
+  float mq = -INFINITY, sq = 0.f, rq = -INFINITY;
+  {
+    int v = tid;
+    for (; v + (kU - 1) * kT < nv; v += kU * kT) {
+      uint4 r0[kU], r1[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) r0[u] = ldg_stream(t4 + v + u * kT);
+#pragma unroll
+      for (int u = 0; u < kU; ++u) r1[u] = ldg_stream(d4 + v + u * kT);
+      online_group<T, kU>(mp, sp, rp, r0, sc);
+      online_group<T, kU>(mq, sq, rq, r1, sc);
+    }
+    for (; v < nv; v += kT) {
+      const uint4 r0[1] = {ldg_stream(t4 + v)};
+      const uint4 r1[1] = {ldg_stream(d4 + v)};
+      online_group<T, 1>(mp, sp, rp, r0, sc);
+      online_group<T, 1>(mq, sq, rq, r1, sc);
+    }
+    for (int k = nv * kV + tid; k < n; k += kT) {
+      float f[1] = {Elems<T>::one(tp, k)};
+      online<1>(mp, sp, rp, f, sc);
+      f[0] = Elems<T>::one(dp, k);
+      online<1>(mq, sq, rq, f, sc);
+    }
+  }
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) {
+    const float om = __shfl_xor_sync(0xffffffffu, mp, s), os = __shfl_xor_sync(0xffffffffu, sp, s);
+    const float qm = __shfl_xor_sync(0xffffffffu, mq, s), qs = __shfl_xor_sync(0xffffffffu, sq, s);
+    merge(mp, sp, om, os, sc);
+    merge(mq, sq, qm, qs, sc);
+  }
+  rp = warp_max_nan(max_nan(rp, rq));
+  if (lane == 0) {
+    red[0][warp] = mp;
+    red[1][warp] = sp;
+    red[2][warp] = mq;
+    red[3][warp] = sq;
+    red[4][warp] = rp;
+  }
+  __syncthreads();
+  if (warp == 0) {  // merge the warps' normalisers, then push the slice's pair to every CTA of the cluster
+    float Mp = lane < kW ? red[0][lane] : -INFINITY, Sp = lane < kW ? red[1][lane] : 0.f;
+    float Mq = lane < kW ? red[2][lane] : -INFINITY, Sq = lane < kW ? red[3][lane] : 0.f;
+    float raw = lane < kW ? red[4][lane] : -INFINITY;
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) {
+      const float om = __shfl_xor_sync(0xffffffffu, Mp, s), os = __shfl_xor_sync(0xffffffffu, Sp, s);
+      const float qm = __shfl_xor_sync(0xffffffffu, Mq, s), qs = __shfl_xor_sync(0xffffffffu, Sq, s);
+      merge(Mp, Sp, om, os, sc);
+      merge(Mq, Sq, qm, qs, sc);
+    }
+    raw = warp_max_nan(raw);
+    const bool bad = !(raw < INFINITY);  // NaN or +inf in this slice
+    if (lane < CS)
+      dsmem_st_v4(dsmem_map(smem_addr(&x1[rank][0]), static_cast<uint32_t>(lane)), bad ? NAN : Mp, Sp,
+                  bad ? NAN : Mq, Sq);
+  }
 
-  // 2. exponentials relative to the slice max, slice sums
-  float s2[2];
-  s2[0] = exp_rows(sP, nch * kChunk, Mp, sc);
-  s2[1] = exp_rows(sQ, nch * kChunk, Mq, sc);
-  block_reduce<2, false>(s2, red1);
-
-  // 3. cluster exchange of slice normalisers
-  if (tid == 0) x1 = Xch1{Mp, s2[0], Mq, s2[1]};
+  // 2. cluster barrier A: every CTA now holds every slice's normalisers
   cluster_sync();
   if (warp == 0) {
-    float mp = -INFINITY, sp = 0.f, mq = -INFINITY, sq = 0.f;
-    if (lane < CS) {
-      const uint32_t base = dsmem_map(smem_addr(&x1), lane);
-      mp = dsmem_ld_f32(base + 0);
-      sp = dsmem_ld_f32(base + 4);
-      mq = dsmem_ld_f32(base + 8);
-      sq = dsmem_ld_f32(base + 12);
-    }
-    const float gmp = warp_max_nan(mp);
-    const float gmq = warp_max_nan(mq);
+    const float m0 = lane < CS ? x1[lane][0] : -INFINITY, s0 = lane < CS ? x1[lane][1] : 0.f;
+    const float m1 = lane < CS ? x1[lane][2] : -INFINITY, s1 = lane < CS ? x1[lane][3] : 0.f;
+    const float gmp = warp_max_nan(m0);
+    const float gmq = warp_max_nan(m1);
     // NaN or +inf anywhere, or a row that is entirely -inf
     const bool bad = !(gmp < INFINITY && gmp > -INFINITY) || !(gmq < INFINITY && gmq > -INFINITY);
     float Sp = 0.f, Sq = 0.f;
     if (!bad) {
-      const float tpv = mp > -INFINITY ? sp * exp2f((mp - gmp) * sc) : 0.f;
-      const float tqv = mq > -INFINITY ? sq * exp2f((mq - gmq) * sc) : 0.f;
+      const float tpv = m0 > -INFINITY ? s0 * fast_exp2((m0 - gmp) * sc) : 0.f;
+      const float tqv = m1 > -INFINITY ? s1 * fast_exp2((m1 - gmq) * sc) : 0.f;
       for (int r = 0; r < CS; ++r) {  // fixed order: identical sums in every CTA
         Sp += __shfl_sync(0xffffffffu, tpv, r);
         Sq += __shfl_sync(0xffffffffu, tqv, r);
       }
     }
     if (lane == 0) {
-      bc[0] = (!bad && Mp > -INFINITY) ? exp2f((Mp - gmp) * sc) / Sp : 0.f;
-      bc[1] = (!bad && Mq > -INFINITY) ? exp2f((Mq - gmq) * sc) / Sq : 0.f;
-      bc[2] = bad ? 1.f : 0.f;
+      bc[0] = bad ? NAN : -gmp * sc;
+      bc[1] = bad ? NAN : Sp;
+      bc[2] = bad ? NAN : -gmq * sc;
+      bc[3] = bad ? NAN : Sq;
     }
   }
   __syncthreads();
-  const float ap = bc[0], aq = bc[1];
-  const bool bad = bc[2] != 0.f;
+  const float ncp0 = bc[0], Sp = bc[1], ncq0 = bc[2], Sq = bc[3];
+  const bool bad = !(Sp > 0.f);
+  const float ncp = ncp0 - __log2f(Sp), ncq = ncq0 - __log2f(Sq);
 
-  // 4. overlaps over the slice
-  float t2[2] = {0.f, 0.f};  // sum min(p,q), sum max(0,p-q)
+  // 3. overlaps over the slice, read again (from L2)
+  float tmin = 0.f, tpp = 0.f;
   if (!bad) {
-    for (int k = tid * 4; k < nch * kChunk; k += kThreads * 4) {
-      const float4 ep = *reinterpret_cast<const float4*>(sP + k);
-      const float4 eq = *reinterpret_cast<const float4*>(sQ + k);
-      const float p0 = ep.x * ap, p1 = ep.y * ap, p2 = ep.z * ap, p3 = ep.w * ap;
-      const float q0 = eq.x * aq, q1 = eq.y * aq, q2 = eq.z * aq, q3 = eq.w * aq;
-      t2[0] += (fminf(p0, q0) + fminf(p1, q1)) + (fminf(p2, q2) + fminf(p3, q3));
-      t2[1] += (fmaxf(p0 - q0, 0.f) + fmaxf(p1 - q1, 0.f)) + (fmaxf(p2 - q2, 0.f) + fmaxf(p3 - q3, 0.f));
+    int v = tid;
+    for (; v + (kU - 1) * kT < nv; v += kU * kT) {
+      uint4 r0[kU], r1[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) r0[u] = ldg_stream(t4 + v + u * kT);
+#pragma unroll
+      for (int u = 0; u < kU; ++u) r1[u] = ldg_stream(d4 + v + u * kT);
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        float f[kV], g[kV];
+        Elems<T>::widen(r0[u], f);
+        Elems<T>::widen(r1[u], g);
+        overlap<kV>(f, g, sc, ncp, ncq, tmin, tpp);
+      }
+    }
+    for (; v < nv; v += kT) {
+      float f[kV], g[kV];
+      Elems<T>::widen(ldg_stream(t4 + v), f);
+      Elems<T>::widen(ldg_stream(d4 + v), g);
+      overlap<kV>(f, g, sc, ncp, ncq, tmin, tpp);
+    }
+    for (int k = nv * kV + tid; k < n; k += kT) {
+      const float f[1] = {Elems<T>::one(tp, k)};
+      const float g[1] = {Elems<T>::one(dp, k)};
+      overlap<1>(f, g, sc, ncp, ncq, tmin, tpp);
     }
   }
-  block_reduce<2, false>(t2, red2);
-  const int x = __ldg(a.ids + o);
-  if (tid == 0) {
-    float px = -1.f, qx = -1.f;
-    if (!bad && x >= lo && x < lo + n) {
-      px = sP[x - lo] * ap;
-      qx = sQ[x - lo] * aq;
-    }
-    x2 = Xch2{t2[0], t2[1], 0.f, px, qx};
+  tpp = warp_sum(tpp - tmin);  // sum max(0, p - q) = sum p - sum min(p, q)
+  tmin = warp_sum(tmin);
+  if (lane == 0) {
+    red[0][warp] = tmin;
+    red[1][warp] = tpp;
   }
-  cluster_sync();
+  __syncthreads();
+  if (warp == 0) {
+    float bt = lane < kW ? red[0][lane] : 0.f, zt = lane < kW ? red[1][lane] : 0.f;
+    for (int s = 16; s > 0; s >>= 1) {
+      bt += __shfl_xor_sync(0xffffffffu, bt, s);
+      zt += __shfl_xor_sync(0xffffffffu, zt, s);
+    }
+    if (lane == 0) {
+      float px = -1.f, qx = -1.f;
+      if (!bad && owner) {
+        px = fast_exp2(fmaf(lpx, sc, ncp0)) / Sp;
+        qx = fast_exp2(fmaf(lqx, sc, ncq0)) / Sq;
+      }
+      dsmem_st_v4(dsmem_map(smem_addr(&x2[rank][0]), 0u), bt, zt, px, qx);
+    }
+  }
 
-  // 5. combine and write (rank 0)
+  // 4. cluster barrier B; rank 0 combines the slices in rank order and writes the statistics
+  cluster_sync();
   if (rank == 0 && warp == 0) {
-    float rb = 0.f, rz = 0.f;
-    if (lane < CS) {
-      const uint32_t base = dsmem_map(smem_addr(&x2), lane);
-      rb = dsmem_ld_f32(base + 0);
-      rz = dsmem_ld_f32(base + 4);
-    }
     float Bt = 0.f, Zt = 0.f;
+    const float rb = lane < CS ? x2[lane][0] : 0.f, rz = lane < CS ? x2[lane][1] : 0.f;
     for (int r = 0; r < CS; ++r) {
       Bt += __shfl_sync(0xffffffffu, rb, r);
       Zt += __shfl_sync(0xffffffffu, rz, r);
@@ -305,26 +266,23 @@ __global__ void __launch_bounds__(kThreads, 2) stats_rows_kernel(const VerifyPar
     const bool xok = x >= 0 && x < a.V;
     if (lane == 0) {
       if (bad || !xok) {
-        write_stats(a, o, NAN, NAN, NAN, NAN, NAN);
+        write_stats(a, pos, NAN, NAN, NAN, NAN, NAN);
         atomicOr(a.ws.err, bad ? kErrNonfinite : kErrToken);
       } else {
-        const uint32_t base = dsmem_map(smem_addr(&x2), static_cast<uint32_t>(x / a.L));
-        const float px = dsmem_ld_f32(base + 12);
-        const float qx = dsmem_ld_f32(base + 16);
-        const float ratio = px >= qx ? 1.f : px / qx;  // min(1, p/q); q = 0 < p gives 1
-        write_stats(a, o, Bt, px, qx, px > 0.f ? ratio : 0.f, Zt);
+        const int owner = x / a.L;
+        const float pxr = x2[owner][2], qxr = x2[owner][3];
+        const float ratio = pxr >= qxr ? 1.f : pxr / qxr;  // min(1, p/q); q = 0 < p gives 1
+        write_stats(a, pos, Bt, pxr, qxr, pxr > 0.f ? ratio : 0.f, Zt);
       }
     }
   }
-  cluster_sync();  // keeps every CTA's shared memory alive until the cluster is done with it
 }
 
 template <typename T>
-static cudaError_t launch_one(const VerifyParams& p, int cs, int smem, cudaStream_t stream) {
+static cudaError_t launch_one(const VerifyParams& p, int cs, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>((long long)p.B * p.G * cs), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.blockDim = dim3(kT, 1, 1);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -337,18 +295,15 @@ static cudaError_t launch_one(const VerifyParams& p, int cs, int smem, cudaStrea
 }
 
 template <typename T>
-static cudaError_t prepare_one(int smem) {
-  cudaError_t e = cudaFuncSetAttribute(stats_rows_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
+static cudaError_t prepare_one() {
   return cudaFuncSetAttribute(stats_rows_kernel<T>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
 }
 
 template <typename T>
-static cudaError_t clusters_one(int cs, int smem, int* out) {
+static cudaError_t clusters_one(int cs, int* out) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(cs * 1024), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.blockDim = dim3(kT, 1, 1);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
@@ -359,16 +314,14 @@ static cudaError_t clusters_one(int cs, int smem, int* out) {
   return cudaOccupancyMaxActiveClusters(out, stats_rows_kernel<T>, &cfg);
 }
 
-cudaError_t stats_prepare(int dtype, int smem) {
-  return dtype == 0 ? prepare_one<float>(smem) : prepare_one<__nv_bfloat16>(smem);
+cudaError_t stats_prepare(int dtype) { return dtype == 0 ? prepare_one<float>() : prepare_one<__nv_bfloat16>(); }
+
+cudaError_t stats_max_active_clusters(int dtype, int cs, int* out) {
+  return dtype == 0 ? clusters_one<float>(cs, out) : clusters_one<__nv_bfloat16>(cs, out);
 }
 
-cudaError_t stats_max_active_clusters(int dtype, int cs, int smem, int* out) {
-  return dtype == 0 ? clusters_one<float>(cs, smem, out) : clusters_one<__nv_bfloat16>(cs, smem, out);
-}
-
-cudaError_t stats_launch(const VerifyParams& p, int dtype, int cs, int smem, cudaStream_t stream) {
-  return dtype == 0 ? launch_one<float>(p, cs, smem, stream) : launch_one<__nv_bfloat16>(p, cs, smem, stream);
+cudaError_t stats_launch(const VerifyParams& p, int dtype, int cs, cudaStream_t stream) {
+  return dtype == 0 ? launch_one<float>(p, cs, stream) : launch_one<__nv_bfloat16>(p, cs, stream);
 }
 
 }  // namespace specv
