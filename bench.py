@@ -349,7 +349,7 @@ def run_ours(a, rank, world, dist):
         "metric": METRIC, "value": units / t_max, "unit": UNIT, "n_gpus": world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded Philox workload, see workloads/)",
-        "config": {**workload_desc(w), "l2": "inputs larger than L2 (1.71 GB vs 129 MB); no flush",
+        "config": {**workload_desc(w), "l2": f"inputs larger than L2 ({nbytes / 1e9:.2f} GB read per step vs 129 MB of L2); no flush",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "rows_per_s": w.B * a.steps * world / t_max,
         "GB_per_s": step_gbs,
