@@ -324,7 +324,10 @@ def run_ours(a, rank, world, dist):
                             max(10, a.steps), 3, stream)
     stats_ms = time_device(lambda: S.accept_stats(w.target, w.draft, w.ids, w.T, w.draft_len, workspace=ws),
                            max(10, a.steps), 3, stream)
+    s_logits, s_u = W.sampler_rows(w)               # the draft-side sampler over every draft row
+    sampler_ms = time_device(lambda: S.sample_rows(s_logits, s_u, w.T), max(10, a.steps), 3, stream)
     esz = 4 if w.dtype == "f32" else 2
+    sampler_bytes = s_logits.shape[0] * w.V * esz   # every row once (the drawn slice again is on top)
     greedy_bytes = (w.B + pos) * w.V * esz          # target rows 0..gamma_b
     stats_bytes = 2 * pos * w.V * esz               # target and draft rows 0..gamma_b-1
     assert S.check_status(ws) == 0
@@ -368,7 +371,9 @@ def run_ours(a, rank, world, dist):
         "variants": {"greedy_ms_per_call": greedy_ms,
                      "greedy_GB_per_s": greedy_bytes / (greedy_ms * 1e-3) / 1e9,
                      "stats_ms_per_call": stats_ms,
-                     "stats_GB_per_s": stats_bytes / (stats_ms * 1e-3) / 1e9},
+                     "stats_GB_per_s": stats_bytes / (stats_ms * 1e-3) / 1e9,
+                     "sampler_rows": int(s_logits.shape[0]), "sampler_ms_per_call": sampler_ms,
+                     "sampler_GB_per_s": sampler_bytes / (sampler_ms * 1e-3) / 1e9},
         "also": also,
     }
     if rank == 0 and not a.no_cpu_baseline:

@@ -148,6 +148,28 @@ int spec_verify_sample_noalloc(const void* target_logits, const void* draft_logi
                                float temperature, int B, int gamma, int V,
                                int32_t* emitted, int32_t* n_accepted, void* stream);
 
+/* Draft-side sampler: the step before verification, Algorithm 1 Phase 1
+ * (paper-graph-ui teardown §2.3 "Algorithm Walkthrough": each guess is drawn
+ * from the approximation model's distribution, x ~ q).  For each row r of
+ * `logits`, q = softmax(logits[r, :] / T) (temperature standardisation, §2.2)
+ * and tokens[r] is the inverse-CDF draw driven by uniforms[r]: the smallest
+ * token k whose running weight sum exceeds uniforms[r] * (total weight), the
+ * same draw spec_verify_sample makes for its bonus token.
+ *
+ *   logits       [R, V]  dtype (the draft model's logits at one position, one row per sequence)
+ *   uniforms     [R]     float32 in [0, 1)
+ *   temperature  > 0, finite
+ *   tokens       [R]     int32 out: the drawn token, or -1 for an invalid row
+ *   workspace    >= spec_workspace_size(R, 0, V, dtype) bytes, 256-byte aligned, zero at rest
+ *
+ * Two kernel launches: the streaming pass of spec_verify_sample over the rows,
+ * then one CTA per row that re-reads only the vocabulary slice holding the
+ * draw.  A row holding NaN / +inf or only -inf, or whose uniform lies outside
+ * [0, 1), gets -1 and is recorded in the workspace's error word. */
+int spec_sample_rows(const void* logits, int dtype, const float* uniforms, float temperature,
+                     int R, int V, int32_t* tokens,
+                     void* workspace, size_t ws_bytes, void* stream);
+
 /* Greedy verification: argmax standardisation (paper-graph-ui teardown §2.2;
  * multigrid.ai on sampling temperature).  a_i = argmax_k target[b,i,k], lowest
  * index on ties; guesses are accepted while a_i == draft_ids[b,i]; the emitted

@@ -260,6 +260,33 @@ def verify_sample(target, draft, dtype, ids, draft_len, uniforms, T, rows=None):
                 valid=valid, candidates=candidates)
 
 
+def sample_rows(logits, dtype, uniforms, T, rows=None):
+    """spec_sample_rows's contract: x ~ softmax(l / T) per row by R2's inverse CDF [p1 §2.3 Phase 1, §2.2].
+
+    logits [R, V] (float32, or bfloat16 bits as uint16), uniforms [R].  Rows with an invalid logit row
+    (R7) or a uniform outside [0, 1) get -1.  Returns tokens, boundary (R8) and candidates per row.
+    """
+    logits = np.asarray(logits)
+    uniforms = np.asarray(uniforms)
+    R = logits.shape[0]
+    idx = range(R) if rows is None else rows
+    out = {"tokens": np.full(R, -1, np.int64), "boundary": np.zeros(R, bool), "valid": np.zeros(R, bool),
+           "candidates": {}}
+    for r in idx:
+        l = widen(logits[r], dtype)
+        u = float(uniforms[r])
+        if not (row_is_valid(l) and 0.0 <= u < 1.0):
+            continue
+        w = softmax_t(l, T)
+        k, flagged = inverse_cdf(w, u)
+        out["tokens"][r] = k
+        out["boundary"][r] = flagged
+        out["valid"][r] = True
+        if flagged:
+            out["candidates"][r] = draw_candidates(w, u)
+    return out
+
+
 def verify_greedy(target, dtype, ids, draft_len, rows=None):
     """spec_verify_greedy's contract, row by row (R5)."""
     B, G1, V = target.shape

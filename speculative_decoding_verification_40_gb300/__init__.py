@@ -10,6 +10,7 @@ fails if the library has not been built
 Entry points (same names as the C ABI, without the spec_ prefix):
   verify_sample  -- accept test, first rejection, residual / bonus draw
   verify_greedy  -- argmax verification
+  sample_rows    -- draft-side sampler: x ~ softmax(l / T) per row by the inverse CDF
   accept_stats   -- per-position beta, p(x), q(x), min(1, p/q), residual mass
   check_status   -- device-side error word of a workspace
 """
@@ -21,7 +22,7 @@ import os
 import torch
 
 __all__ = [
-    "SpecVerifyError", "verify_sample", "verify_greedy", "accept_stats", "check_status", "workspace_size",
+    "SpecVerifyError", "verify_sample", "verify_greedy", "sample_rows", "accept_stats", "check_status", "workspace_size",
     "workspace_for", "plan", "LIB_PATH", "lib",
 ]
 
@@ -52,6 +53,8 @@ def _load() -> ctypes.CDLL:
         fn = getattr(L, name)
         fn.argtypes = [vp, vp, i32, vp, vp, vp, f32, i32, i32, i32, vp, vp, vp, sz, vp]
         fn.restype = i32
+    L.spec_sample_rows.argtypes = [vp, i32, vp, f32, i32, i32, vp, vp, sz, vp]
+    L.spec_sample_rows.restype = i32
     L.spec_verify_greedy.argtypes = [vp, vp, i32, vp, vp, i32, i32, i32, vp, vp, vp, sz, vp]
     L.spec_verify_greedy.restype = i32
     L.spec_accept_stats.argtypes = [vp, vp, i32, vp, vp, f32, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]
@@ -196,6 +199,27 @@ def verify_sample(target: torch.Tensor, draft: torch.Tensor, ids: torch.Tensor, 
     if check:
         check_status(ws)
     return emitted, n_accepted
+
+
+def sample_rows(logits: torch.Tensor, uniforms: torch.Tensor, temperature: float, *, tokens=None,
+                workspace: torch.Tensor | None = None, check: bool = False) -> torch.Tensor:
+    """spec_sample_rows: logits [R, V], uniforms [R] float32; returns tokens [R] int32."""
+    if logits.dim() != 2:
+        raise ValueError("logits must be [R, V]")
+    R, V = logits.shape
+    _cuda(logits, "logits")
+    _cuda(uniforms, "uniforms", torch.float32, (R,))
+    dev = logits.device
+    if tokens is None:
+        tokens = torch.empty(R, dtype=torch.int32, device=dev)
+    _cuda(tokens, "tokens", torch.int32, (R,))
+    ws = workspace if workspace is not None else workspace_for(dev, workspace_size(R, 0, V, logits.dtype))
+    code = lib.spec_sample_rows(_p(logits), _dtype_code(logits), _p(uniforms), float(temperature), R, V,
+                                _p(tokens), _p(ws), ws.numel(), _stream(dev))
+    _raise(code, "spec_sample_rows")
+    if check:
+        check_status(ws)
+    return tokens
 
 
 def verify_greedy(target: torch.Tensor, ids: torch.Tensor, draft_len: torch.Tensor | None = None,

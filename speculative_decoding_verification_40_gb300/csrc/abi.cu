@@ -323,6 +323,32 @@ int spec_accept_stats(const void* target_logits, const void* draft_logits, int d
                     true);
 }
 
+int spec_sample_rows(const void* logits, int dtype, const float* uniforms, float temperature, int R, int V,
+                     int32_t* tokens, void* workspace, size_t ws_bytes, void* stream) {
+  int st = check_common(dtype, R, 0, V, workspace, ws_bytes);
+  if (st != SPEC_OK) return st;
+  if (!(std::isfinite(temperature) && temperature > 0.f)) return SPEC_ERR_ARG;
+  if (R == 0) return SPEC_OK;
+  if (logits == nullptr || uniforms == nullptr || tokens == nullptr) return SPEC_ERR_ARG;
+  const int esz = dtype == SPEC_F32 ? 4 : 2;
+  specv::SampleParams p = {};
+  p.target = logits;
+  p.uniforms = uniforms;
+  p.scale = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+  p.B = R;
+  p.G = 0;
+  p.V = V;
+  p.slice = sample_slice(V, dtype);
+  p.nslices = (V + p.slice - 1) / p.slice;
+  p.dslice = p.slice;
+  p.ndslices = p.nslices;
+  p.vec = rows_aligned(logits, V, esz) ? 1 : 0;
+  p.emitted = tokens;
+  p.n_acc = nullptr;
+  p.ws = specv::ws_carve(workspace, R, 0, V);
+  return launch_status(specv::rows_sample_launch(p, dtype, static_cast<cudaStream_t>(stream)));
+}
+
 int spec_verify_greedy(const void* target_logits, const void* draft_logits, int dtype, const int32_t* draft_ids,
                        const int32_t* draft_len, int B, int gamma, int V, int32_t* emitted, int32_t* n_accepted,
                        void* workspace, size_t ws_bytes, void* stream) {

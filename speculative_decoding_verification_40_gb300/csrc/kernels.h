@@ -62,6 +62,8 @@ cudaError_t stats_max_active_clusters(int dtype, int cs, int* out);
 cudaError_t stats_launch(const VerifyParams& p, int dtype, int cs, cudaStream_t stream);
 // phases: 1 = stream kernel, 2 = draw kernel, 3 = both
 cudaError_t sample_launch(const SampleParams& p, int dtype, int phases, cudaStream_t stream);
+// stream kernel (gamma = 0) then one sampling CTA per row; emitted is the [B] token output
+cudaError_t rows_sample_launch(const SampleParams& p, int dtype, cudaStream_t stream);
 cudaError_t greedy_launch(const GreedyParams& p, int dtype, cudaStream_t stream);
 
 }  // namespace specv

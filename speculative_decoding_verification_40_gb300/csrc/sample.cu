@@ -340,34 +340,18 @@ __device__ void resolve_row(const SampleParams& a, int b, int gb, const RowState
 
 // ----------------------------------------------------------------------------- stream kernel
 
+// Online normalisers (m, S) of n logits of one row (and of a second row when has_q), this thread's
+// share: 16-byte vectors when vec, in groups of U per row in flight, then a scalar tail.  raw tracks the
+// NaN-propagating maximum of the raw logits (NaN / +inf detection).
 template <typename T>
-__global__ void __launch_bounds__(kStreamThreads, 4) verify_stream_kernel(const SampleParams a) {
-  __shared__ float red[4][kSW];
-  __shared__ float rawr[kSW];
+__device__ __forceinline__ void slice_normalisers(const T* __restrict__ tp, const T* __restrict__ dp, bool has_q,
+                                                  int n, bool vec, float sc, float& mp, float& sp, float& rp,
+                                                  float& mq, float& sq, float& rq) {
   constexpr int kV = Elems<T>::kVec;
   constexpr int U = 4;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // the draw kernel may be scheduled once every stream CTA is running; it waits for their results
-  asm volatile("griddepcontrol.launch_dependents;");
-  const int NS = a.nslices;
-  const int s = blockIdx.x % NS;
-  const int pos = blockIdx.x / NS;
-  const int G1 = a.G + 1;
-  const int b = pos / G1;
-  const int i = pos - b * G1;
-  const int gb = a.draft_len ? __ldg(a.draft_len + b) : a.G;
-  if (gb < 0 || gb > a.G || i > gb) return;  // invalid length (the draw kernel reports it) or padding
-  const bool has_q = i < gb;
-  const float sc = a.scale;
-  const int lo = s * a.slice;
-  const int n = min(a.V, lo + a.slice) - lo;
-  const T* tp = reinterpret_cast<const T*>(a.target) + ((size_t)b * G1 + i) * a.V + lo;
-  const T* dp = has_q ? reinterpret_cast<const T*>(a.draft) + ((size_t)b * a.G + i) * a.V + lo : tp;
-
-  float mp = -INFINITY, sp = 0.f, rp = -INFINITY;
-  float mq = -INFINITY, sq = 0.f, rq = -INFINITY;
+  const int tid = threadIdx.x;
   int done = 0;
-  if (a.vec) {
+  if (vec) {
     const int nv = n / kV;
     const uint4* t4 = reinterpret_cast<const uint4*>(tp);
     const uint4* d4 = reinterpret_cast<const uint4*>(dp);
@@ -410,8 +394,14 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_stream_kernel(const 
       online<1>(mq, sq, rq, f, sc);
     }
   }
+}
 
-  // block merge of the normalisers (fixed order, identical for p and q)
+// Block merge of the threads' normalisers in a fixed order (identical for p and q): warp shuffles, then
+// thread 0 over the warps.  Thread 0 returns the block's (m_p, S_p, m_q, S_q) and raw maximum.
+__device__ __forceinline__ void block_normalisers(float mp, float sp, float rp, float mq, float sq, float rq,
+                                                  float sc, float (*red)[kSW], float* rawr, float4& out,
+                                                  float& raw) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float om = __shfl_xor_sync(0xffffffffu, mp, o), os = __shfl_xor_sync(0xffffffffu, sp, o);
@@ -428,6 +418,46 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_stream_kernel(const 
     rawr[warp] = rp;
   }
   __syncthreads();
+  if (tid == 0) {
+    float Mp = red[0][0], Sp = red[1][0], Mq = red[2][0], Sq = red[3][0], r = rawr[0];
+    for (int w = 1; w < kSW; ++w) {
+      merge(Mp, Sp, red[0][w], red[1][w], sc);
+      merge(Mq, Sq, red[2][w], red[3][w], sc);
+      r = max_nan(r, rawr[w]);
+    }
+    out = make_float4(Mp, Sp, Mq, Sq);
+    raw = r;
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kStreamThreads, 4) verify_stream_kernel(const SampleParams a) {
+  __shared__ float red[4][kSW];
+  __shared__ float rawr[kSW];
+  const int tid = threadIdx.x;
+  // the draw kernel may be scheduled once every stream CTA is running; it waits for their results
+  asm volatile("griddepcontrol.launch_dependents;");
+  const int NS = a.nslices;
+  const int s = blockIdx.x % NS;
+  const int pos = blockIdx.x / NS;
+  const int G1 = a.G + 1;
+  const int b = pos / G1;
+  const int i = pos - b * G1;
+  const int gb = a.draft_len ? __ldg(a.draft_len + b) : a.G;
+  if (gb < 0 || gb > a.G || i > gb) return;  // invalid length (the draw kernel reports it) or padding
+  const bool has_q = i < gb;
+  const float sc = a.scale;
+  const int lo = s * a.slice;
+  const int n = min(a.V, lo + a.slice) - lo;
+  const T* tp = reinterpret_cast<const T*>(a.target) + ((size_t)b * G1 + i) * a.V + lo;
+  const T* dp = has_q ? reinterpret_cast<const T*>(a.draft) + ((size_t)b * a.G + i) * a.V + lo : tp;
+
+  float mp = -INFINITY, sp = 0.f, rp = -INFINITY;
+  float mq = -INFINITY, sq = 0.f, rq = -INFINITY;
+  slice_normalisers<T>(tp, dp, has_q, n, a.vec != 0, sc, mp, sp, rp, mq, sq, rq);
+  float4 nrm;
+  float raw;
+  block_normalisers(mp, sp, rp, mq, sq, rq, sc, red, rawr, nrm, raw);
   if (tid == 32 && has_q) {  // the logits at the draft token, if this slice holds it
     const int x = __ldg(a.ids + (size_t)b * a.G + i);
     if (x >= lo && x < lo + n)
@@ -435,14 +465,9 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_stream_kernel(const 
           make_float2(Elems<T>::one(tp, x - lo), Elems<T>::one(dp, x - lo));
   }
   if (tid == 0) {
-    float Mp = red[0][0], Sp = red[1][0], Mq = red[2][0], Sq = red[3][0], raw = rawr[0];
-    for (int w = 1; w < kSW; ++w) {
-      merge(Mp, Sp, red[0][w], red[1][w], sc);
-      merge(Mq, Sq, red[2][w], red[3][w], sc);
-      raw = max_nan(raw, rawr[w]);
-    }
     const bool bad = !(raw < INFINITY);  // NaN or +inf in this slice
-    reinterpret_cast<float4*>(a.ws.part)[(size_t)pos * NS + s] = make_float4(bad ? NAN : Mp, Sp, bad ? NAN : Mq, Sq);
+    reinterpret_cast<float4*>(a.ws.part)[(size_t)pos * NS + s] =
+        make_float4(bad ? NAN : nrm.x, nrm.y, bad ? NAN : nrm.z, nrm.w);
   }
 }
 
@@ -555,6 +580,360 @@ static cudaError_t launch_draw(const SampleParams& p, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, verify_draw_kernel<T>, p);
+}
+
+// ----------------------------------------------------------------------------- row sampler
+
+// One CTA per row b of logits [R, V] (launched after the stream kernel with gamma = 0, which left the
+// row's slice normalisers in the workspace): x ~ softmax(l / T) by the inverse CDF with uniforms[b].
+// The slice holding the draw is picked from the slice masses S_s 2^((m_s - M) log2(e)/T) of the stream
+// pass, so only that slice is read again; inside it the weights w = 2^(l log2(e)/T - M log2(e)/T) give
+// chunk masses, then warp scans find the token.  If rounding leaves the target beyond the slice's
+// recomputed mass, the draw is the slice's last token of positive weight.
+namespace {
+
+template <typename T>
+__device__ __forceinline__ void row_weights(const T* row, bool vec, int base, int n, float sc, float nm,
+                                            float (&w)[Elems<T>::kVec]) {
+  constexpr int kV = Elems<T>::kVec;
+  float f[kV];
+  if (vec && base + kV <= n) {
+    Elems<T>::widen(__ldg(reinterpret_cast<const uint4*>(row + base)), f);
+  } else {
+#pragma unroll
+    for (int j = 0; j < kV; ++j) f[j] = base + j < n ? Elems<T>::one(row, base + j) : -INFINITY;
+  }
+#pragma unroll
+  for (int j = 0; j < kV; ++j) w[j] = fast_exp2(fmaf(f[j], sc, nm));
+}
+
+}  // namespace
+
+// Inverse-CDF draw inside one slice of n logits (the whole CTA calls it): chunk masses of the weights
+// w = 2^(l sc + nm) into cm, then warp 0 finds the chunk and the token whose running sum first exceeds t.
+// If rounding leaves t beyond the slice's mass the draw is the slice's last token of positive weight.
+// Returns the token's index in the slice in warp 0 (-1 elsewhere, or if the slice has no positive weight).
+template <typename T>
+__device__ int draw_in_slice(const T* srow, int n, bool vec, float sc, float nm, float t, float* cm) {
+  constexpr int kV = Elems<T>::kVec;
+  constexpr int kCpc = kR * 32 * kV;  // elements per chunk: kR vectors per lane
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nch = (n + kCpc - 1) / kCpc;
+  for (int c = warp; c < nch; c += kSW) {
+    float acc = 0.f;
+#pragma unroll
+    for (int r = 0; r < kR; ++r) {
+      float w[kV];
+      row_weights<T>(srow, vec, c * kCpc + (r * 32 + lane) * kV, n, sc, nm, w);
+#pragma unroll
+      for (int j = 0; j < kV; ++j) acc += w[j];
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) cm[c] = acc;
+  }
+  __syncthreads();
+  if (warp != 0) return -1;
+
+  int chunk = -1, lastc = -1;
+  float carry = 0.f;
+  for (int g = 0; g * 32 < nch; ++g) {
+    const int c = g * 32 + lane;
+    const float v = c < nch ? cm[c] : 0.f;
+    const float incl = carry + warp_inclusive_scan(v, lane);
+    const unsigned hit = __ballot_sync(0xffffffffu, incl > t);
+    const unsigned pos = __ballot_sync(0xffffffffu, v > 0.f);
+    if (pos) lastc = g * 32 + 31 - __clz(pos);
+    if (hit && chunk < 0) {
+      const int l0 = __ffs(hit) - 1;
+      chunk = g * 32 + l0;
+      t -= __shfl_sync(0xffffffffu, incl - v, l0);
+    }
+    carry = __shfl_sync(0xffffffffu, incl, 31);
+  }
+  const bool fallback = chunk < 0;
+  if (fallback) chunk = lastc;  // t beyond the slice's mass: the last chunk of positive mass
+  int token = -1, lastk = -1;
+  if (chunk >= 0) {
+    float cc = 0.f;
+    for (int r = 0; r < kR && token < 0; ++r) {
+      const int base = chunk * kCpc + (r * 32 + lane) * kV;
+      float w[kV];
+      row_weights<T>(srow, vec, base, n, sc, nm, w);
+      float ls = 0.f;
+#pragma unroll
+      for (int j = 0; j < kV; ++j) ls += w[j];
+      const float incl = cc + warp_inclusive_scan(ls, lane);
+      int lpos = -1;  // this lane's last element of positive weight
+#pragma unroll
+      for (int j = 0; j < kV; ++j)
+        if (w[j] > 0.f) lpos = j;
+      const unsigned pos = __ballot_sync(0xffffffffu, lpos >= 0);
+      if (pos) {
+        const int l1 = 31 - __clz(pos);
+        lastk = __shfl_sync(0xffffffffu, base + lpos, l1);
+      }
+      const unsigned hit = fallback ? 0u : __ballot_sync(0xffffffffu, incl > t);
+      if (hit) {
+        const int l0 = __ffs(hit) - 1;
+        int k = -1;
+        if (lane == l0) {  // walk this lane's elements in order
+          float run = incl - ls;
+#pragma unroll
+          for (int j = 0; j < kV; ++j) {
+            run += w[j];
+            if (k < 0 && run > t) k = base + j;
+          }
+          if (k < 0) k = base + lpos;  // rounding inside the lane: its last positive weight
+        }
+        token = __shfl_sync(0xffffffffu, k, l0);
+      }
+      cc = __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (token < 0) token = lastk;  // rounding inside the chunk: its last positive weight
+  }
+  return token;
+}
+
+// Online normaliser (m, S) of a contiguous segment of n logits, merged over the warp (every lane gets
+// it), and the NaN-propagating raw maximum.  16-byte loads when vec, four in flight per lane.
+template <typename T>
+__device__ __forceinline__ void warp_segment(const T* __restrict__ seg, int n, bool vec, float sc, float& m,
+                                             float& sm, float& raw) {
+  constexpr int kV = Elems<T>::kVec;
+  constexpr int U = 4;
+  const int lane = threadIdx.x & 31;
+  m = -INFINITY;
+  sm = 0.f;
+  raw = -INFINITY;
+  if (n > 0) {
+    if (vec) {
+      const uint4* v4 = reinterpret_cast<const uint4*>(seg);
+      const int nv = n / kV;
+      int j = lane;
+      for (; j + (U - 1) * 32 < nv; j += U * 32) {
+        uint4 r[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) r[u] = ldg_stream(v4 + j + u * 32);
+        online_group<T, U>(m, sm, raw, r, sc);
+      }
+      for (; j < nv; j += 32) {
+        const uint4 r[1] = {ldg_stream(v4 + j)};
+        online_group<T, 1>(m, sm, raw, r, sc);
+      }
+    } else {
+      for (int k = lane; k < n; k += 32) {
+        float f[1] = {Elems<T>::one(seg, k)};
+        online<1>(m, sm, raw, f, sc);
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float om = __shfl_xor_sync(0xffffffffu, m, o), os = __shfl_xor_sync(0xffffffffu, sm, o);
+    merge(m, sm, om, os, sc);
+  }
+  raw = warp_max_nan(raw);
+}
+
+// Elements per warp segment of a slice of L elements (eight segments, whole warp-loads each).
+template <typename T>
+__host__ __device__ __forceinline__ int segment_len(int L) {
+  return static_cast<int>(align_up((L + kSW - 1) / kSW, 32 * Elems<T>::kVec));
+}
+
+// Rows that fit one slice: one CTA per row, one launch.  Warp w streams the contiguous segment w of
+// the row once for its online normalisers (m_w, S_w); thread 0 combines the eight segments in order,
+// picks the segment holding u * Z from their masses S_w 2^((m_w - M) log2(e)/T), and the CTA draws
+// inside that segment only (its second read, an eighth of the row, hits L2).
+template <typename T>
+__global__ void __launch_bounds__(kST) sample_rows_fused_kernel(const SampleParams a) {
+  __shared__ float segm[kSW], segs[kSW], segr[kSW];
+  __shared__ float cm[kMaxChunksPerSlice];
+  __shared__ float sh_t, sh_m;
+  __shared__ int sh_w, sh_err;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = blockIdx.x;
+  const float sc = a.scale;
+  const int V = a.V;
+  const T* row = reinterpret_cast<const T*>(a.target) + (size_t)b * V;
+  const bool vec = a.vec != 0;
+  const int segE = segment_len<T>(V);
+  {
+    const int lo = warp * segE;
+    float m, sm, raw;
+    warp_segment<T>(row + lo, min(V, lo + segE) - lo, vec, sc, m, sm, raw);
+    if (lane == 0) {
+      segm[warp] = m;
+      segs[warp] = sm;
+      segr[warp] = raw;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float M = segm[0], raw = segr[0];
+    for (int w = 1; w < kSW; ++w) {
+      M = max_nan(M, segm[w]);
+      raw = max_nan(raw, segr[w]);
+    }
+    const float u = __ldg(a.uniforms + b);
+    uint32_t err = 0;
+    if (!(raw < INFINITY) || !(M > -INFINITY)) err |= kErrNonfinite;
+    if (!(u >= 0.f && u < 1.f)) err |= kErrArg;
+    float e[kSW], Z = 0.f;
+    for (int w = 0; w < kSW; ++w) {
+      e[w] = (!err && segm[w] > -INFINITY) ? segs[w] * fast_exp2((segm[w] - M) * sc) : 0.f;
+      Z += e[w];
+    }
+    const float t = u * Z;
+    int sel = -1, last = 0;
+    float before = 0.f, acc = 0.f;
+    for (int w = 0; w < kSW; ++w) {
+      if (e[w] > 0.f) last = w;
+      if (sel < 0 && acc + e[w] > t) {
+        sel = w;
+        before = acc;
+      }
+      acc += e[w];
+    }
+    sh_err = static_cast<int>(err);
+    sh_m = M;
+    sh_w = sel >= 0 ? sel : last;
+    sh_t = sel >= 0 ? t - before : INFINITY;  // beyond every segment: take the last positive weight
+  }
+  __syncthreads();
+  if (sh_err) {
+    if (tid == 0) {
+      a.emitted[b] = -1;
+      atomicOr(a.ws.err, static_cast<uint32_t>(sh_err));
+    }
+    return;
+  }
+  const int lo = sh_w * segE;
+  const int n = min(V, lo + segE) - lo;
+  const int tok = draw_in_slice<T>(row + lo, n, vec, sc, -sh_m * sc, sh_t, cm);
+  if (tid == 0) a.emitted[b] = tok >= 0 ? lo + tok : -1;
+}
+
+// Rows longer than one slice, pass 1: one CTA per (row b, slice s); warp w writes the normaliser of
+// its segment of the slice, (m, S) with m = NaN if the segment holds NaN or +inf, to the workspace's
+// per-row segment list [b][s * 8 + w].
+template <typename T>
+__global__ void __launch_bounds__(kST, 4) sample_stream_kernel(const SampleParams a) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  asm volatile("griddepcontrol.launch_dependents;");
+  const int NS = a.nslices;
+  const int s = blockIdx.x % NS;
+  const int b = blockIdx.x / NS;
+  const int segE = segment_len<T>(a.slice);
+  const int lo = s * a.slice + warp * segE;
+  const int hi = min(a.V, min(s * a.slice + a.slice, lo + segE));
+  float m, sm, raw;
+  warp_segment<T>(reinterpret_cast<const T*>(a.target) + (size_t)b * a.V + lo, hi - lo, a.vec != 0, a.scale, m, sm,
+                  raw);
+  if (lane == 0)
+    reinterpret_cast<float2*>(a.ws.dch)[(size_t)b * chunks_per_row(a.V) + s * kSW + warp] =
+        make_float2(raw < INFINITY ? m : NAN, sm);
+}
+
+// Pass 2: one CTA per row.  The row's NS * 8 segment normalisers (in order) give the segment masses;
+// the segment holding u * Z is read again (an eighth of a slice) for the draw.
+template <typename T>
+__global__ void __launch_bounds__(kST) sample_rows_kernel(const SampleParams a) {
+  __shared__ float cm[kMaxChunksPerSlice];
+  __shared__ float wsum[kSW], wmax[kSW];
+  __shared__ float sh_t;
+  __shared__ int sh_sel;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = blockIdx.x;
+  const int NG = a.nslices * kSW;  // segments of the row, at most 256
+  const float sc = a.scale;
+  // launched as a programmatic dependent of the stream kernel: wait for all of it (and its writes)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  float2* segp = reinterpret_cast<float2*>(a.ws.dch) + (size_t)b * chunks_per_row(a.V);
+  float2 sg = make_float2(-INFINITY, 0.f);
+  if (tid < NG) {
+    sg = __ldcg(segp + tid);
+    segp[tid] = make_float2(0.f, 0.f);  // the workspace goes back to zero
+  }
+  // row max (NaN-propagating), then the masses' inclusive scan in segment order
+  float mx = warp_max_nan(sg.x);
+  if (lane == 0) wmax[warp] = mx;
+  if (tid == 0) sh_sel = -1;
+  __syncthreads();
+  float M = wmax[0];
+  for (int w = 1; w < kSW; ++w) M = max_nan(M, wmax[w]);
+  const float u = __ldg(a.uniforms + b);
+  uint32_t err = 0;
+  if (!(M > -INFINITY && M < INFINITY)) err |= kErrNonfinite;
+  if (!(u >= 0.f && u < 1.f)) err |= kErrArg;
+  const float e = (!err && sg.x > -INFINITY) ? sg.y * fast_exp2((sg.x - M) * sc) : 0.f;
+  const float incl_w = warp_inclusive_scan(e, lane);
+  if (lane == 31) wsum[warp] = incl_w;
+  __syncthreads();
+  float before_w = 0.f, Z = 0.f;
+  for (int w = 0; w < kSW; ++w) {
+    if (w < warp) before_w += wsum[w];
+    Z += wsum[w];
+  }
+  const float t = u * Z;
+  const float incl = before_w + incl_w;  // running mass through segment tid (nondecreasing in tid)
+  // the first segment whose running mass exceeds t is the number of segments whose running mass does not
+  const int first = __syncthreads_count(tid < NG && incl <= t);
+  if (first < NG && tid == first) sh_t = t - (incl - e);
+  if (e > 0.f) atomicMax(&sh_sel, tid);  // the last segment of positive mass (sh_sel started at -1)
+  __syncthreads();
+  if (err) {
+    if (tid == 0) {
+      a.emitted[b] = -1;
+      atomicOr(a.ws.err, err);
+    }
+    return;
+  }
+  // beyond the last segment (rounding at u * Z near Z): the draw is the last positive weight
+  const bool beyond = first >= NG;
+  const int g = beyond ? sh_sel : first;
+  const int s = g / kSW, w = g % kSW;
+  const int segE = segment_len<T>(a.slice);
+  const int lo = s * a.slice + w * segE;
+  const int n = min(a.V, min(s * a.slice + a.slice, lo + segE)) - lo;
+  const T* srow = reinterpret_cast<const T*>(a.target) + (size_t)b * a.V + lo;
+  const int tok = draw_in_slice<T>(srow, n, a.vec != 0, sc, -M * sc, beyond ? INFINITY : sh_t, cm);
+  if (tid == 0) a.emitted[b] = tok >= 0 ? lo + tok : -1;
+}
+
+template <typename T>
+static cudaError_t launch_rows(const SampleParams& p, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.B));
+  cfg.blockDim = dim3(kStreamThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, sample_rows_kernel<T>, p);
+}
+
+cudaError_t rows_sample_launch(const SampleParams& p, int dtype, cudaStream_t stream) {
+  const dim3 block(kStreamThreads);
+  const dim3 g1(static_cast<unsigned>((long long)p.B * p.nslices));
+  cudaError_t e;
+  if (p.nslices == 1) {
+    if (dtype == 0)
+      sample_rows_fused_kernel<float><<<dim3(static_cast<unsigned>(p.B)), block, 0, stream>>>(p);
+    else
+      sample_rows_fused_kernel<__nv_bfloat16><<<dim3(static_cast<unsigned>(p.B)), block, 0, stream>>>(p);
+    return cudaGetLastError();
+  }
+  if (dtype == 0) {
+    sample_stream_kernel<float><<<g1, block, 0, stream>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return launch_rows<float>(p, stream);
+  }
+  sample_stream_kernel<__nv_bfloat16><<<g1, block, 0, stream>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return launch_rows<__nv_bfloat16>(p, stream);
 }
 
 cudaError_t sample_launch(const SampleParams& p, int dtype, int phases, cudaStream_t stream) {

@@ -110,3 +110,24 @@ def test_launch_plans_for_the_five_workloads(B, G, V, bf16, cs, monkeypatch):
     assert p["cluster_size"] == cs
     assert p["slice_len"] * cs >= V and p["slice_len"] % 8 == 0
     assert p["smem_bytes"] <= 227 * 1024
+
+
+def test_sample_rows_rejects_bad_arguments_on_the_host():
+    L = S.lib
+    p = ctypes.c_void_p(4096)
+
+    def call(logits=p, dtype=0, u=p, T=1.0, R=3, V=100, tok=p, ws=FAKE_WS, wsb=BIG):
+        return L.spec_sample_rows(logits, dtype, u, T, R, V, tok, ws, wsb, None)
+
+    assert call(dtype=5) == 2
+    assert call(R=-1) == 1
+    assert call(V=0) == 1
+    assert call(V=262145) == 1
+    assert call(T=0.0) == 1
+    assert call(T=float("nan")) == 1
+    assert call(logits=None) == 1
+    assert call(u=None) == 1
+    assert call(tok=None) == 1
+    assert call(ws=None) == 7
+    assert call(wsb=16) == 7
+    assert call(R=0, logits=None, u=None, tok=None, ws=None, wsb=0) == 0

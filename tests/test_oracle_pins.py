@@ -341,3 +341,49 @@ def test_draw_candidates_cover_the_near_edge_tokens():
     k, flag = O.inverse_cdf(w, u)
     assert flag and k in c
     assert O.draw_candidates(w, 0.25) == [0]
+
+
+# ----------------------------------------------------------------------------- draft-side sampler
+
+def _stratified(N):
+    return ((np.arange(N) + 0.5) / N).astype(np.float64)
+
+
+@pytest.mark.parametrize("T", [1.0, 2.0, 0.5])
+def test_sample_rows_stratified_uniforms_reproduce_the_softmax(T):
+    """Inverse CDF over a stratified grid u_j = (j + 1/2)/N hits token k floor- or ceil(N p_k) times,
+    with p_k = w_k^(1/T) / sum w^(1/T) for logits log w (closed form, not the oracle's softmax)."""
+    wts = np.array([1.0, 4.0, 0.5, 2.5, 0.0, 8.0, 1e-3])
+    with np.errstate(divide="ignore"):
+        l = np.log(wts).astype(np.float32)
+    N = 20000
+    R = N
+    logits = np.tile(l, (R, 1))
+    out = O.sample_rows(logits, "f32", _stratified(N), T)
+    counts = np.bincount(out["tokens"], minlength=wts.size)
+    pw = wts ** (1.0 / T)
+    p = pw / pw.sum()
+    assert counts[4] == 0                                # zero weight is never drawn
+    assert np.all(np.abs(counts - N * p) <= 1.0 + 1e-6 * N), (counts, N * p)
+
+
+def test_sample_rows_edges():
+    l = np.array([[0.0, 0.0, -np.inf, 0.0],              # u = 0 draws the first positive weight
+                  [0.0, 0.0, -np.inf, 0.0],              # u just below 1 draws the last positive weight
+                  [np.nan, 0.0, 0.0, 0.0],               # invalid row
+                  [-np.inf] * 4,                         # all -inf: invalid
+                  [0.0, 1.0, 2.0, 3.0]], dtype=np.float32)
+    u = np.array([0.0, np.nextafter(np.float32(1), np.float32(0)), 0.5, 0.5, 1.0], dtype=np.float32)
+    out = O.sample_rows(l, "f32", u, 1.0)
+    assert list(out["tokens"]) == [0, 3, -1, -1, -1]     # u = 1 is outside [0, 1)
+
+
+def test_sample_rows_is_the_bonus_draw_of_verification():
+    """gamma = 0 verification emits exactly the sampler's draw (same inverse CDF, same uniform)."""
+    rng = np.random.default_rng(7)
+    l = rng.normal(0, 2, size=(6, 50)).astype(np.float32)
+    u = rng.random(6).astype(np.float32)
+    out = O.sample_rows(l, "f32", u, 0.8)
+    ver = O.verify_sample(l[:, None, :], np.zeros((6, 0, 50), np.float32), "f32", np.zeros((6, 0), np.int64),
+                          None, u[:, None], 0.8)
+    assert list(out["tokens"]) == [int(e[0]) for e in ver["emitted"]]

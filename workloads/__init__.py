@@ -111,6 +111,20 @@ def _uniforms(B: int, gamma: int, k: int, call: int, device) -> torch.Tensor:
     return uniform_f32((B, gamma + 1), UNIFORM_SEED, 100 + k + 16 * call, device)
 
 
+def sampler_rows(w: "Workload", call: int = 0):
+    """Inputs of the draft-side sampler on workload w: its draft logit rows (b, i) with i < gamma_b as an
+    [R, V] tensor, and one uniform per row (Philox stream 200 + k + 16 * call)."""
+    V = w.V
+    if w.draft_len is None:
+        rows = w.draft.reshape(-1, V)
+    else:
+        keep = (torch.arange(w.gamma, device=w.draft.device)[None, :] < w.draft_len[:, None]).reshape(-1)
+        rows = w.draft.reshape(-1, V)[keep]
+    k = int(w.name.lstrip("c"))
+    u = uniform_f32((rows.shape[0],), UNIFORM_SEED, 200 + k + 16 * call, rows.device)
+    return rows.contiguous(), u
+
+
 def load_c2_sigma() -> list[float] | None:
     if not os.path.exists(C2_SIGMA_FILE):
         return None
