@@ -197,6 +197,26 @@ int spec_accept_stats(const void* target_logits, const void* draft_logits, int d
                       float* resid_mass,
                       void* workspace, size_t ws_bytes, void* stream);
 
+/* Planning helpers (paper-graph-ui teardown §3.1-§3.5).  Host functions, no CUDA call.
+ *   spec_expected_tokens:      E[# tokens per step] = (1 - alpha^(gamma+1)) / (1 - alpha)   (Eq. 1;
+ *                              gamma + 1 at alpha = 1).  NaN for alpha outside [0, 1] or gamma < 0.
+ *   spec_walltime_improvement: Theorem 3.8, E[# tokens] / (gamma c + 1), c = cost of M_q / cost of M_p.
+ *   spec_operations_factor:    Theorem 3.11, (gamma c_hat + gamma + 1) / E[# tokens].
+ *   spec_optimal_gamma:        gamma* = argmax over gamma in [1, max_gamma] of Theorem 3.8 (§3.5: every
+ *                              gamma is evaluated; ties go to the smaller gamma); writes the improvement at
+ *                              gamma* to *improvement if not NULL.  -1 for invalid arguments. */
+double spec_expected_tokens(double alpha, int gamma);
+double spec_walltime_improvement(double alpha, int gamma, double c);
+double spec_operations_factor(double alpha, int gamma, double c_hat);
+int spec_optimal_gamma(double alpha, double c, int max_gamma, double* improvement);
+
+/* Corpus acceptance rate alpha = E[beta] (Corollary 3.6): the mean of the finite entries of the device
+ * array beta[0, n) (for instance the beta output of spec_accept_stats, where NaN marks positions that
+ * were not verified), accumulated in double in a fixed order.  out is a device pointer to two doubles:
+ * out[0] = alpha (NaN if there is no finite entry), out[1] = the number of finite entries.  One kernel
+ * launch on `stream`; returns SPEC_ERR_ARG for n < 0 or NULL pointers. */
+int spec_alpha_mean(const float* beta, long long n, double* out, void* stream);
+
 /* Synchronises `stream`, reads and clears the workspace's error word, and
  * returns the lowest-numbered spec_status_t it records (SPEC_OK if none). */
 int spec_check_status(void* workspace, void* stream);

@@ -384,3 +384,22 @@ def walltime_improvement(alpha: float, gamma: int, c: float) -> float:
 def operations_factor(alpha: float, gamma: int, c_hat: float) -> float:
     """Thm 3.11 [p1 "Number of Arithmetic Operations"]."""
     return (gamma * c_hat + gamma + 1.0) / expected_tokens(alpha, gamma)
+
+
+def optimal_gamma(alpha: float, c: float, max_gamma: int) -> int:
+    """gamma* = argmax over gamma in 1..max_gamma of Thm 3.8's improvement [p1 §3.5 "Choosing gamma"],
+    by evaluating every gamma as that section prescribes; ties go to the smaller gamma."""
+    best, best_v = 1, walltime_improvement(alpha, 1, c)
+    for g in range(2, max_gamma + 1):
+        v = walltime_improvement(alpha, g, c)
+        if v > best_v:
+            best, best_v = g, v
+    return best
+
+
+def alpha_from_beta(beta) -> tuple[float, int]:
+    """alpha = E[beta] over a corpus of positions [p1 Corollary 3.6]: the mean of the finite beta values
+    (NaN marks positions that were not verified), and how many there were."""
+    b = np.asarray(beta, dtype=np.float64).reshape(-1)
+    b = b[np.isfinite(b)]
+    return (float(b.mean()) if b.size else float("nan")), int(b.size)

@@ -23,7 +23,8 @@ import torch
 
 __all__ = [
     "SpecVerifyError", "verify_sample", "verify_greedy", "sample_rows", "accept_stats", "check_status", "workspace_size",
-    "workspace_for", "plan", "LIB_PATH", "lib",
+    "workspace_for", "plan", "LIB_PATH", "lib", "expected_tokens", "walltime_improvement", "operations_factor",
+    "optimal_gamma", "alpha_mean",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libspecverify.so")
@@ -59,6 +60,17 @@ def _load() -> ctypes.CDLL:
     L.spec_verify_greedy.restype = i32
     L.spec_accept_stats.argtypes = [vp, vp, i32, vp, vp, f32, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]
     L.spec_accept_stats.restype = i32
+    dbl, i64 = ctypes.c_double, ctypes.c_longlong
+    L.spec_expected_tokens.argtypes = [dbl, i32]
+    L.spec_expected_tokens.restype = dbl
+    L.spec_walltime_improvement.argtypes = [dbl, i32, dbl]
+    L.spec_walltime_improvement.restype = dbl
+    L.spec_operations_factor.argtypes = [dbl, i32, dbl]
+    L.spec_operations_factor.restype = dbl
+    L.spec_optimal_gamma.argtypes = [dbl, dbl, i32, ctypes.POINTER(dbl)]
+    L.spec_optimal_gamma.restype = i32
+    L.spec_alpha_mean.argtypes = [vp, i64, vp, vp]
+    L.spec_alpha_mean.restype = i32
     L.spec_check_status.argtypes = [vp, vp]
     L.spec_check_status.restype = i32
     ip = ctypes.POINTER(ctypes.c_int)
@@ -138,6 +150,39 @@ def plan(B: int, gamma: int, V: int, dtype: torch.dtype = torch.float32) -> dict
     _raise(lib.spec_verify_plan(B, gamma, V, code, ctypes.byref(cs), ctypes.byref(L), ctypes.byref(sm),
                                 ctypes.byref(g)), "spec_verify_plan")
     return {"cluster_size": cs.value, "slice_len": L.value, "smem_bytes": sm.value, "greedy_ctas_per_row": g.value}
+
+
+def expected_tokens(alpha: float, gamma: int) -> float:
+    """spec_expected_tokens: (1 - alpha^(gamma+1)) / (1 - alpha)."""
+    return float(lib.spec_expected_tokens(alpha, gamma))
+
+
+def walltime_improvement(alpha: float, gamma: int, c: float) -> float:
+    """spec_walltime_improvement (Theorem 3.8)."""
+    return float(lib.spec_walltime_improvement(alpha, gamma, c))
+
+
+def operations_factor(alpha: float, gamma: int, c_hat: float) -> float:
+    """spec_operations_factor (Theorem 3.11)."""
+    return float(lib.spec_operations_factor(alpha, gamma, c_hat))
+
+
+def optimal_gamma(alpha: float, c: float, max_gamma: int = 64) -> tuple[int, float]:
+    """spec_optimal_gamma: (gamma*, improvement at gamma*)."""
+    v = ctypes.c_double()
+    g = int(lib.spec_optimal_gamma(alpha, c, max_gamma, ctypes.byref(v)))
+    if g < 0:
+        raise ValueError("alpha must lie in [0, 1], c >= 0, max_gamma >= 1")
+    return g, v.value
+
+
+def alpha_mean(beta: torch.Tensor) -> tuple[float, int]:
+    """spec_alpha_mean: alpha = mean of the finite beta values (device reduction), and their count."""
+    _cuda(beta, "beta", torch.float32)
+    out = torch.empty(2, dtype=torch.float64, device=beta.device)
+    _raise(lib.spec_alpha_mean(_p(beta), beta.numel(), _p(out), _stream(beta.device)), "spec_alpha_mean")
+    o = out.cpu()
+    return float(o[0]), int(o[1])
 
 
 def check_status(workspace: torch.Tensor | None = None, device=None, raise_on_error: bool = True) -> int:

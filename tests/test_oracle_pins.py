@@ -387,3 +387,32 @@ def test_sample_rows_is_the_bonus_draw_of_verification():
     ver = O.verify_sample(l[:, None, :], np.zeros((6, 0, 50), np.float32), "f32", np.zeros((6, 0), np.int64),
                           None, u[:, None], 0.8)
     assert list(out["tokens"]) == [int(e[0]) for e in ver["emitted"]]
+
+
+# ----------------------------------------------------------------------------- gamma* (§3.5) and alpha (Cor. 3.6)
+
+@pytest.mark.parametrize("row", _rows("gamma_star.txt"), ids=lambda r: f"a{r[0]}c{r[1]}")
+def test_optimal_gamma_matches_pages(row):
+    alpha, c, g = float(row[0]), float(row[1]), int(row[2])
+    assert O.optimal_gamma(alpha, c, 200) == g
+
+
+def test_gamma_one_improvement_is_corollary_39():
+    """Cor. 3.9: at gamma = 1 the improvement factor is (1 + alpha)/(1 + c)."""
+    rng = np.random.default_rng(4)
+    for alpha, c in rng.random((50, 2)):
+        assert O.walltime_improvement(alpha, 1, c) == pytest.approx((1 + alpha) / (1 + c), rel=1e-13)
+
+
+def test_optimal_gamma_without_draft_cost_is_the_cap():
+    """c = 0: the factor grows with gamma for alpha < 1, so the search returns its upper end."""
+    for alpha in (0.3, 0.8, 0.95):
+        assert O.optimal_gamma(alpha, 0.0, 17) == 17
+
+
+def test_alpha_is_the_mean_of_finite_beta():
+    b = np.array([[0.5, 0.7, np.nan], [0.9, np.nan, np.nan]])
+    a, n = O.alpha_from_beta(b)
+    assert n == 3 and a == pytest.approx(0.7, abs=1e-15)
+    a, n = O.alpha_from_beta(np.full(4, np.nan))
+    assert n == 0 and np.isnan(a)
