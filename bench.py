@@ -324,6 +324,13 @@ def run_ours(a, rank, world, dist):
                             max(10, a.steps), 3, stream)
     stats_ms = time_device(lambda: S.accept_stats(w.target, w.draft, w.ids, w.T, w.draft_len, workspace=ws),
                            max(10, a.steps), 3, stream)
+    # the byte-lean early exit on the same batch: same outputs, logits read only up to each row's rejection
+    early_ms = time_device(lambda: S.verify_sample(w.target, w.draft, w.ids, w.uniforms, w.T, w.draft_len,
+                                                   emitted=em, n_accepted=na, workspace=ws, phase="early_exit"),
+                           max(10, a.steps), 3, stream)
+    n_b = na.long()
+    g_b = w.draft_len.long() if w.draft_len is not None else torch.full_like(n_b, w.gamma)
+    early_rows = int(((n_b + 1) + torch.where(n_b < g_b, n_b + 1, g_b)).sum())
     s_logits, s_u = W.sampler_rows(w)               # the draft-side sampler over every draft row
     sampler_ms = time_device(lambda: S.sample_rows(s_logits, s_u, w.T), max(10, a.steps), 3, stream)
     esz = 4 if w.dtype == "f32" else 2
@@ -372,6 +379,9 @@ def run_ours(a, rank, world, dist):
                      "greedy_GB_per_s": greedy_bytes / (greedy_ms * 1e-3) / 1e9,
                      "stats_ms_per_call": stats_ms,
                      "stats_GB_per_s": stats_bytes / (stats_ms * 1e-3) / 1e9,
+                     "early_exit_ms_per_call": early_ms,
+                     "early_exit_rows_read": early_rows, "all_positions_rows_read": w.B + 2 * pos,
+                     "early_exit_GB_per_s": early_rows * w.V * esz / (early_ms * 1e-3) / 1e9,
                      "sampler_rows": int(s_logits.shape[0]), "sampler_ms_per_call": sampler_ms,
                      "sampler_GB_per_s": sampler_bytes / (sampler_ms * 1e-3) / 1e9},
         "also": also,

@@ -122,6 +122,25 @@ int spec_verify_sample_draw(const void* target_logits, const void* draft_logits,
                             int32_t* emitted, int32_t* n_accepted,
                             void* workspace, size_t ws_bytes, void* stream);
 
+/* Byte-lean early exit: spec_verify_sample that reads position i + 1 of a batch
+ * row only while the row has not stopped.  Positions are verified one after
+ * the other (one streaming launch per position, gamma + 1 in all, then the
+ * draw launch); after each, the row stops at its first rejection, at an
+ * invalid position, or at the bonus position gamma_b.  The logits read per row
+ * are then the n + 1 target and n + 1 draft rows up to the first rejection n
+ * (n + 1 target and n draft rows for a bonus draw) instead of 2 gamma_b + 1:
+ * about sum_k alpha^k rows when each guess is accepted with probability alpha
+ * (§3.1).  For valid inputs the outputs are exactly spec_verify_sample's (the
+ * same arithmetic decides every position and draws).  A logit row after the
+ * first rejection is never read, so a NaN / +inf or all -inf row there does
+ * not make the batch row invalid as it does in spec_verify_sample.  Arguments,
+ * layouts, workspace and the other errors as spec_verify_sample. */
+int spec_verify_sample_early_exit(const void* target_logits, const void* draft_logits, int dtype,
+                                  const int32_t* draft_ids, const int32_t* draft_len, const float* uniforms,
+                                  float temperature, int B, int gamma, int V,
+                                  int32_t* emitted, int32_t* n_accepted,
+                                  void* workspace, size_t ws_bytes, void* stream);
+
 /* spec_verify_sample without a workspace argument, for callers that cannot
  * allocate device memory: for instance a plugin handed only its input and
  * output buffers by a host program that owns every allocator, or a serving loop

@@ -50,7 +50,8 @@ def _load() -> ctypes.CDLL:
     L.spec_workspace_size.restype = sz
     L.spec_workspace_init.argtypes = [vp, sz, vp]
     L.spec_workspace_init.restype = i32
-    for name in ("spec_verify_sample", "spec_verify_sample_stream", "spec_verify_sample_draw"):
+    for name in ("spec_verify_sample", "spec_verify_sample_stream", "spec_verify_sample_draw",
+                 "spec_verify_sample_early_exit"):
         fn = getattr(L, name)
         fn.argtypes = [vp, vp, i32, vp, vp, vp, f32, i32, i32, i32, vp, vp, vp, sz, vp]
         fn.restype = i32
@@ -224,6 +225,8 @@ def verify_sample(target: torch.Tensor, draft: torch.Tensor, ids: torch.Tensor, 
 
     phase="stream" / "draw" calls spec_verify_sample_stream / spec_verify_sample_draw: the two halves
     of the same computation, to be called in that order with the same arguments and workspace.
+    phase="early_exit" calls spec_verify_sample_early_exit (same results, reads rows only up to the
+    first rejection).
     """
     B, G, V = _common(target, draft, ids, draft_len)
     _cuda(uniforms, "uniforms", torch.float32, (B, G + 1))
@@ -236,7 +239,7 @@ def verify_sample(target: torch.Tensor, draft: torch.Tensor, ids: torch.Tensor, 
     _cuda(n_accepted, "n_accepted", torch.int32, (B,))
     ws = workspace if workspace is not None else workspace_for(dev, workspace_size(B, G, V, target.dtype))
     fn = {"both": lib.spec_verify_sample, "stream": lib.spec_verify_sample_stream,
-          "draw": lib.spec_verify_sample_draw}[phase]
+          "draw": lib.spec_verify_sample_draw, "early_exit": lib.spec_verify_sample_early_exit}[phase]
     code = fn(_p(target), _p(draft) if G > 0 else None, _dtype_code(target), _p(ids) if G > 0 else None,
               _p(draft_len), _p(uniforms), float(temperature), B, G, V, _p(emitted), _p(n_accepted), _p(ws),
               ws.numel(), _stream(dev))

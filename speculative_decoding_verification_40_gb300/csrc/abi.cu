@@ -186,6 +186,27 @@ int draw_slice(int B, int V, int dtype) {
   return slice;
 }
 
+// Early exit streams one position at a time, so a launch holds only the rows still verifying: slices
+// are cut so that the first position gives about four CTAs per SM (at most 32 slices per row, whole
+// draw chunks).  SPECVERIFY_EE_SLICE (elements) overrides within the same limits.
+int early_exit_slice(int B, int V, int dtype) {
+  const int chunk = 4 * 32 * (dtype == SPEC_F32 ? 4 : 8);
+  const long long want_ctas = 4LL * (device_sms() > 0 ? device_sms() : 152);
+  long long ns = (want_ctas + B - 1) / (B > 0 ? B : 1);
+  if (ns < 1) ns = 1;
+  if (ns > specv::kMaxSlices) ns = specv::kMaxSlices;
+  int slice = static_cast<int>((V + ns - 1) / ns);
+  if (const char* env = std::getenv("SPECVERIFY_EE_SLICE")) {
+    const int w = std::atoi(env);
+    if (w > 0) slice = w;
+  }
+  const int lo = (V + specv::kMaxSlices - 1) / specv::kMaxSlices;
+  if (slice < lo) slice = lo;
+  slice = static_cast<int>(align_up(slice, chunk));
+  if (slice > specv::kMaxChunksPerSlice * chunk) slice = specv::kMaxChunksPerSlice * chunk;
+  return slice;
+}
+
 bool rows_aligned(const void* p, int V, int esz) {
   return (reinterpret_cast<uintptr_t>(p) % 16 == 0) && ((static_cast<size_t>(V) * esz) % 16 == 0);
 }
@@ -217,7 +238,8 @@ int launch_status(cudaError_t e) {
 int run_verify(const void* target, const void* draft, int dtype, const int32_t* ids, const int32_t* draft_len,
                const float* uniforms, float temperature, int B, int gamma, int V, int32_t* emitted,
                int32_t* n_accepted, float* beta, float* p_draft, float* q_draft, float* accept_prob,
-               float* resid, void* workspace, size_t ws_bytes, void* stream, bool stats, int phases = 3) {
+               float* resid, void* workspace, size_t ws_bytes, void* stream, bool stats, int phases = 3,
+               bool early_exit = false) {
   int st = check_common(dtype, B, gamma, V, workspace, ws_bytes);
   if (st != SPEC_OK) return st;
   if (!(std::isfinite(temperature) && temperature > 0.f)) return SPEC_ERR_ARG;
@@ -247,6 +269,11 @@ int run_verify(const void* target, const void* draft, int dtype, const int32_t* 
     p.emitted = emitted;
     p.n_acc = n_accepted;
     p.ws = specv::ws_carve(workspace, B, gamma, V);
+    if (early_exit) {
+      p.slice = early_exit_slice(B, V, dtype);
+      p.nslices = (V + p.slice - 1) / p.slice;
+      return launch_status(specv::sample_early_exit_launch(p, dtype, static_cast<cudaStream_t>(stream)));
+    }
     return launch_status(specv::sample_launch(p, dtype, phases, static_cast<cudaStream_t>(stream)));
   }
 
@@ -321,6 +348,15 @@ int spec_accept_stats(const void* target_logits, const void* draft_logits, int d
   return run_verify(target_logits, draft_logits, dtype, draft_ids, draft_len, nullptr, temperature, B, gamma, V,
                     nullptr, nullptr, beta, p_draft, q_draft, accept_prob, resid_mass, workspace, ws_bytes, stream,
                     true);
+}
+
+int spec_verify_sample_early_exit(const void* target_logits, const void* draft_logits, int dtype,
+                                  const int32_t* draft_ids, const int32_t* draft_len, const float* uniforms,
+                                  float temperature, int B, int gamma, int V, int32_t* emitted,
+                                  int32_t* n_accepted, void* workspace, size_t ws_bytes, void* stream) {
+  return run_verify(target_logits, draft_logits, dtype, draft_ids, draft_len, uniforms, temperature, B, gamma, V,
+                    emitted, n_accepted, nullptr, nullptr, nullptr, nullptr, nullptr, workspace, ws_bytes, stream,
+                    false, 3, true);
 }
 
 int spec_sample_rows(const void* logits, int dtype, const float* uniforms, float temperature, int R, int V,

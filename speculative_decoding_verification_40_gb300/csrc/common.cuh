@@ -41,6 +41,7 @@ struct Workspace {
   float* xl;                 // [B, G] float2 target / draft logit at the draft token
   float* dsum;               // [B, kMaxSlices] float2 mass of each draw slice (residual, p)
   float* dch;                // [B, chunks] float2 mass of each chunk of the drawn row(s)
+  int* stop;                 // [B] early exit: 0 while row b is verifying, n + 1 once it stopped at n
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -52,7 +53,7 @@ __host__ __device__ inline size_t ws_bytes_for(int B, int G, int V) {
   const size_t P = (size_t)B * (size_t)(G + 1);
   return 256 + align_up((size_t)B * 4, 256) + align_up(P * 8, 256) + align_up(P * kMaxSlices * 16, 256) +
          align_up((size_t)B * G * 8, 256) + align_up((size_t)B * kMaxSlices * 8, 256) +
-         align_up((size_t)B * chunks_per_row(V) * 8, 256);
+         align_up((size_t)B * chunks_per_row(V) * 8, 256) + align_up((size_t)B * 4, 256);
 }
 
 inline Workspace ws_carve(void* base, int B, int G, int V) {
@@ -72,6 +73,8 @@ inline Workspace ws_carve(void* base, int B, int G, int V) {
   w.dsum = reinterpret_cast<float*>(p);
   p += align_up((size_t)B * kMaxSlices * 8, 256);
   w.dch = reinterpret_cast<float*>(p);
+  p += align_up((size_t)B * chunks_per_row(V) * 8, 256);
+  w.stop = reinterpret_cast<int*>(p);
   return w;
 }
 

@@ -51,6 +51,7 @@ struct SampleParams {
   int dslice;                // vocabulary elements per draw CTA (a multiple of the draw chunk)
   int ndslices;              // draw CTAs per batch row (<= kMaxSlices)
   int vec;                   // every logit row starts on a 16-byte boundary
+  int step;                  // 0: stream every position; i + 1: stream position i of the rows still verifying
   int32_t* emitted;          // [B, G+1]
   int32_t* n_acc;            // [B]
   Workspace ws;
@@ -62,6 +63,8 @@ cudaError_t stats_max_active_clusters(int dtype, int cs, int* out);
 cudaError_t stats_launch(const VerifyParams& p, int dtype, int cs, cudaStream_t stream);
 // phases: 1 = stream kernel, 2 = draw kernel, 3 = both
 cudaError_t sample_launch(const SampleParams& p, int dtype, int phases, cudaStream_t stream);
+// early exit: stream kernel once per position (p.step = i + 1, rows still verifying only), then the draw
+cudaError_t sample_early_exit_launch(SampleParams p, int dtype, cudaStream_t stream);
 // stream kernel (gamma = 0) then one sampling CTA per row; emitted is the [B] token output
 cudaError_t rows_sample_launch(const SampleParams& p, int dtype, cudaStream_t stream);
 cudaError_t greedy_launch(const GreedyParams& p, int dtype, cudaStream_t stream);

@@ -94,6 +94,42 @@ struct DrawSmem {
 };
 
 // Accept decisions of row b from the slice normalisers: the same arithmetic in every CTA of the row.
+// Row normalisers of one position from its NS slice partials (m_p, S_p, m_q, S_q), combined by one warp
+// in a fixed order, so every caller gets the same values bit for bit.  Every lane returns them.
+__device__ __forceinline__ float4 position_norm(const float4* __restrict__ part_pos, int NS, float sc) {
+  const int lane = threadIdx.x & 31;
+  float4 pr = make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+  if (lane < NS) pr = __ldcg(part_pos + lane);
+  const float Mp = warp_max_nan(pr.x);
+  const float Mq = warp_max_nan(pr.z);
+  const float tp = (pr.x > -INFINITY && Mp < INFINITY) ? pr.y * fast_exp2((pr.x - Mp) * sc) : 0.f;
+  const float tq = (pr.z > -INFINITY && Mq < INFINITY) ? pr.w * fast_exp2((pr.z - Mq) * sc) : 0.f;
+  float Sp = 0.f, Sq = 0.f;
+  for (int r = 0; r < NS; ++r) {
+    Sp += __shfl_sync(0xffffffffu, tp, r);
+    Sq += __shfl_sync(0xffffffffu, tq, r);
+  }
+  return make_float4(Mp, Sp, Mq, Sq);
+}
+
+// Accept test of guess i < gamma_b of row b, u_i <= min(1, p(x_i)/q(x_i)) with p(x_i) > 0, from the
+// position's normalisers and the logits at the draft token; err collects what makes the row invalid.
+__device__ __forceinline__ int accept_position(const SampleParams& a, int b, int i, float4 nm, uint32_t& err) {
+  const int x = __ldg(a.ids + (size_t)b * a.G + i);
+  const float ui = __ldg(a.uniforms + (size_t)b * (a.G + 1) + i);
+  if (!(nm.x > -INFINITY && nm.x < INFINITY)) err |= kErrNonfinite;
+  if (!(nm.z > -INFINITY && nm.z < INFINITY)) err |= kErrNonfinite;
+  if (x < 0 || x >= a.V) err |= kErrToken;
+  if (!(ui >= 0.f && ui < 1.f)) err |= kErrArg;
+  if (err) return 0;
+  const float sc = a.scale;
+  const float2 xl = __ldcg(reinterpret_cast<const float2*>(a.ws.xl) + (size_t)b * a.G + i);
+  const float px = fast_exp2((xl.x - nm.x) * sc) / nm.y;
+  const float qx = fast_exp2((xl.y - nm.z) * sc) / nm.w;
+  const float ratio = px >= qx ? 1.f : px / qx;  // min(1, p/q); q = 0 < p gives 1
+  return (px > 0.f && ui <= ratio) ? 1 : 0;
+}
+
 __device__ RowState decide_row(const SampleParams& a, int b, int gb, DrawSmem& sm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G1 = a.G + 1;
@@ -102,22 +138,12 @@ __device__ RowState decide_row(const SampleParams& a, int b, int gb, DrawSmem& s
   const float4* part = reinterpret_cast<const float4*>(a.ws.part) + (size_t)b * G1 * NS;
   // per-position normalisers from the slice partials (fixed combination order)
   for (int i = warp; i <= gb; i += kSW) {
-    float4 pr = make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
-    if (lane < NS) pr = __ldcg(part + (size_t)i * NS + lane);
-    const float Mp = warp_max_nan(pr.x);
-    const float Mq = warp_max_nan(pr.z);
-    const float tp = (pr.x > -INFINITY && Mp < INFINITY) ? pr.y * fast_exp2((pr.x - Mp) * sc) : 0.f;
-    const float tq = (pr.z > -INFINITY && Mq < INFINITY) ? pr.w * fast_exp2((pr.z - Mq) * sc) : 0.f;
-    float Sp = 0.f, Sq = 0.f;
-    for (int r = 0; r < NS; ++r) {
-      Sp += __shfl_sync(0xffffffffu, tp, r);
-      Sq += __shfl_sync(0xffffffffu, tq, r);
-    }
+    const float4 nm = position_norm(part + (size_t)i * NS, NS, sc);
     if (lane == 0) {
-      sm.mp[i] = Mp;
-      sm.sp[i] = Sp;
-      sm.mq[i] = Mq;
-      sm.sq[i] = Sq;
+      sm.mp[i] = nm.x;
+      sm.sp[i] = nm.y;
+      sm.mq[i] = nm.z;
+      sm.sq[i] = nm.w;
     }
   }
   if (tid == 0) sm.err = 0;
@@ -128,20 +154,10 @@ __device__ RowState decide_row(const SampleParams& a, int b, int gb, DrawSmem& s
   if (tid <= gb) {
     const int i = tid;
     int code = 1;
-    if (!(sm.mp[i] > -INFINITY && sm.mp[i] < INFINITY)) err |= kErrNonfinite;
     if (i < gb) {
-      const int x = __ldg(a.ids + (size_t)b * a.G + i);
-      const float ui = __ldg(U + i);
-      if (!(sm.mq[i] > -INFINITY && sm.mq[i] < INFINITY)) err |= kErrNonfinite;
-      if (x < 0 || x >= a.V) err |= kErrToken;
-      if (!(ui >= 0.f && ui < 1.f)) err |= kErrArg;
-      if (!err) {
-        const float2 xl = __ldcg(reinterpret_cast<const float2*>(a.ws.xl) + (size_t)b * a.G + i);
-        const float px = fast_exp2((xl.x - sm.mp[i]) * sc) / sm.sp[i];
-        const float qx = fast_exp2((xl.y - sm.mq[i]) * sc) / sm.sq[i];
-        const float ratio = px >= qx ? 1.f : px / qx;  // min(1, p/q); q = 0 < p gives 1
-        code = (px > 0.f && ui <= ratio) ? 1 : 0;
-      }
+      code = accept_position(a, b, i, make_float4(sm.mp[i], sm.sp[i], sm.mq[i], sm.sq[i]), err);
+    } else if (!(sm.mp[i] > -INFINITY && sm.mp[i] < INFINITY)) {
+      err |= kErrNonfinite;
     }
     sm.acc[i] = err ? -1 : code;
   }
@@ -333,7 +349,10 @@ __device__ void resolve_row(const SampleParams& a, int b, int gb, const RowState
   for (int k = tid; k < gb; k += kST) reinterpret_cast<float2*>(a.ws.xl)[(size_t)b * a.G + k] = make_float2(0.f, 0.f);
   for (int k = tid; k < ND * cps; k += kST) dch[k] = make_float2(0.f, 0.f);
   for (int k = tid; k < ND; k += kST) dsum[k] = make_float2(0.f, 0.f);
-  if (tid == 0) a.ws.ticket[b] = 0u;
+  if (tid == 0) {
+    a.ws.ticket[b] = 0u;
+    a.ws.stop[b] = 0;
+  }
 }
 
 }  // namespace
@@ -434,17 +453,30 @@ template <typename T>
 __global__ void __launch_bounds__(kStreamThreads, 4) verify_stream_kernel(const SampleParams a) {
   __shared__ float red[4][kSW];
   __shared__ float rawr[kSW];
+  __shared__ int last;
   const int tid = threadIdx.x;
   // the draw kernel may be scheduled once every stream CTA is running; it waits for their results
   asm volatile("griddepcontrol.launch_dependents;");
   const int NS = a.nslices;
   const int s = blockIdx.x % NS;
-  const int pos = blockIdx.x / NS;
   const int G1 = a.G + 1;
-  const int b = pos / G1;
-  const int i = pos - b * G1;
+  int b, i;
+  if (a.step) {  // early exit: position step - 1 of row b, unless the row already stopped
+    b = blockIdx.x / NS;
+    i = a.step - 1;
+  } else {
+    const int p = blockIdx.x / NS;
+    b = p / G1;
+    i = p - b * G1;
+  }
+  const int pos = b * G1 + i;
   const int gb = a.draft_len ? __ldg(a.draft_len + b) : a.G;
   if (gb < 0 || gb > a.G || i > gb) return;  // invalid length (the draw kernel reports it) or padding
+  if (a.step) {
+    // launched as a programmatic dependent of the previous position's launch: wait for its decisions
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (__ldcg(a.ws.stop + b) != 0) return;
+  }
   const bool has_q = i < gb;
   const float sc = a.scale;
   const int lo = s * a.slice;
@@ -468,6 +500,26 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_stream_kernel(const 
     const bool bad = !(raw < INFINITY);  // NaN or +inf in this slice
     reinterpret_cast<float4*>(a.ws.part)[(size_t)pos * NS + s] =
         make_float4(bad ? NAN : nrm.x, nrm.y, bad ? NAN : nrm.z, nrm.w);
+  }
+  if (!a.step) return;
+  // early exit: the last CTA of (b, i) decides guess i -- the draw kernel's test, same arithmetic -- and
+  // stops the row at a rejection, an invalid position or the bonus position gamma_b
+  if (tid == 0 || tid == 32) __threadfence();
+  __syncthreads();
+  if (tid == 0) last = atomicAdd(a.ws.ticket + b, 1u) == static_cast<unsigned>(NS - 1);
+  __syncthreads();
+  if (!last || tid >= 32) return;
+  __threadfence();
+  const float4 nm = position_norm(reinterpret_cast<const float4*>(a.ws.part) + (size_t)pos * NS, NS, sc);
+  if (tid == 0) {
+    a.ws.ticket[b] = 0u;
+    bool stop = i == gb;
+    if (!stop) {
+      uint32_t err = 0;
+      const int code = accept_position(a, b, i, nm, err);
+      stop = err != 0 || code == 0;
+    }
+    if (stop) a.ws.stop[b] = i + 1;
   }
 }
 
@@ -580,6 +632,26 @@ static cudaError_t launch_draw(const SampleParams& p, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, verify_draw_kernel<T>, p);
+}
+
+cudaError_t sample_early_exit_launch(SampleParams p, int dtype, cudaStream_t stream) {
+  for (int i = 0; i <= p.G; ++i) {
+    p.step = i + 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((long long)p.B * p.nslices));
+    cfg.blockDim = dim3(kStreamThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = i > 0 ? 1 : 0;  // each position's launch overlaps the previous one's tail
+    const cudaError_t e = dtype == 0 ? cudaLaunchKernelEx(&cfg, verify_stream_kernel<float>, p)
+                                     : cudaLaunchKernelEx(&cfg, verify_stream_kernel<__nv_bfloat16>, p);
+    if (e != cudaSuccess) return e;
+  }
+  p.step = 0;
+  return dtype == 0 ? launch_draw<float>(p, stream) : launch_draw<__nv_bfloat16>(p, stream);
 }
 
 // ----------------------------------------------------------------------------- row sampler
