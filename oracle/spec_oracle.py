@@ -47,6 +47,12 @@ the design notes):
   R8  boundary draws: a row is flagged when a tested uniform lies within 1e-5
       of its acceptance threshold, or the final uniform lies within 1e-5 of a
       CDF edge of the chosen token (both on the normalised scale).
+  R9  top-k keeps every token whose logit is >= the k-th largest logit (ties at
+      the boundary are all kept); fewer than k finite logits keep everything.
+  R10 nucleus (top-p) keeps every token whose logit is >= that of the token at
+      which the descending running probability first reaches top_p (ties kept);
+      top_p >= 1 keeps everything.  A standardised row is the logit row with
+      the dropped tokens set to -inf, so p is renormalised over the kept set.
 """
 from __future__ import annotations
 
@@ -84,6 +90,48 @@ def softmax_t(logits: np.ndarray, T: float) -> np.ndarray:
     m = np.max(z)
     e = np.exp(z - m)
     return e / np.sum(e)
+
+
+# ----------------------------------------------------------------------------- top-k / nucleus (R9, R10)
+
+def topk_threshold(logits: np.ndarray, k: int) -> float:
+    """Top-k standardisation [p1 §2.2]: keep the k largest probabilities, zero the rest, renormalise.
+
+    Softmax is increasing in the logit, so the k largest probabilities are the k largest logits.  R9:
+    the kept set is every token whose logit is >= tau, the k-th largest logit (ties at tau are all
+    kept); tau = -inf (keep everything) when fewer than k logits are finite.
+    """
+    fin = np.sort(logits[np.isfinite(logits)])[::-1]
+    if k > fin.size:
+        return float("-inf")
+    return float(fin[k - 1])
+
+
+def topp_threshold(logits: np.ndarray, T: float, top_p: float):
+    """Nucleus standardisation [p1 §2.2]: sort the probabilities descending, keep the shortest prefix
+    whose cumulative mass reaches top_p, zero the rest, renormalise.
+
+    R10: tau is the logit of the token at which the running mass first reaches top_p (ties at tau are
+    all kept); tau = -inf when top_p >= 1.  Returns (tau, flagged): flagged when the running mass at
+    that token or at the one before lies within 1e-5 of top_p, where float32 and float64 sums may pick
+    different tokens (counted, like R8's boundary draws).
+    """
+    if top_p >= 1.0:
+        return float("-inf"), False
+    p = softmax_t(logits, T)
+    order = np.argsort(-p, kind="stable")
+    c = np.cumsum(p[order])
+    j = int(np.searchsorted(c, top_p, side="left"))      # first running mass >= top_p
+    j = min(j, p.size - 1)
+    flagged = abs(c[j] - top_p) < BOUNDARY_EPS or (j > 0 and abs(c[j - 1] - top_p) < BOUNDARY_EPS)
+    return float(logits[order[j]]), bool(flagged)
+
+
+def apply_threshold(logits: np.ndarray, tau: float) -> np.ndarray:
+    """Logits below tau become -inf (probability 0 after the softmax); NaN stays NaN."""
+    out = np.array(logits, dtype=np.float64, copy=True)
+    out[out < tau] = -np.inf
+    return out
 
 
 # ----------------------------------------------------------------------------- one row
@@ -227,8 +275,11 @@ def _draft_len(draft_len, B, gamma):
     return np.asarray(draft_len, dtype=np.int64)
 
 
-def verify_sample(target, draft, dtype, ids, draft_len, uniforms, T, rows=None):
+def verify_sample(target, draft, dtype, ids, draft_len, uniforms, T, rows=None, tthr=None, dthr=None):
     """spec_verify_sample's contract, row by row.  target [B,gamma+1,V], draft [B,gamma,V].
+
+    tthr [B,gamma+1] / dthr [B,gamma] (float32, optional) standardise each logit row first: logits
+    below the row's threshold are dropped (top-k / nucleus, R9 / R10), as spec_verify_sample_masked.
 
     `rows` restricts the work to a subset of b (the outputs still have B rows;
     rows not computed hold -2).  Returns dict of numpy arrays: emitted
@@ -249,6 +300,10 @@ def verify_sample(target, draft, dtype, ids, draft_len, uniforms, T, rows=None):
         gb = int(gl[b])
         tb = widen(target[b], dtype)
         db = widen(draft[b], dtype) if gamma > 0 else np.zeros((0, V))
+        if tthr is not None:
+            tb = np.stack([apply_threshold(tb[i], float(np.float32(tthr[b][i]))) for i in range(G1)])
+        if dthr is not None and gamma > 0:
+            db = np.stack([apply_threshold(db[i], float(np.float32(dthr[b][i]))) for i in range(gamma)])
         res = verify_row(tb, db, ids[b], gb, u[b], float(np.float32(T)))
         emitted[b] = res["emitted"]
         n_acc[b] = res["n"]
@@ -260,7 +315,7 @@ def verify_sample(target, draft, dtype, ids, draft_len, uniforms, T, rows=None):
                 valid=valid, candidates=candidates)
 
 
-def sample_rows(logits, dtype, uniforms, T, rows=None):
+def sample_rows(logits, dtype, uniforms, T, rows=None, thr=None):
     """spec_sample_rows's contract: x ~ softmax(l / T) per row by R2's inverse CDF [p1 §2.3 Phase 1, §2.2].
 
     logits [R, V] (float32, or bfloat16 bits as uint16), uniforms [R].  Rows with an invalid logit row
@@ -274,6 +329,8 @@ def sample_rows(logits, dtype, uniforms, T, rows=None):
            "candidates": {}}
     for r in idx:
         l = widen(logits[r], dtype)
+        if thr is not None:
+            l = apply_threshold(l, float(np.float32(thr[r])))
         u = float(uniforms[r])
         if not (row_is_valid(l) and 0.0 <= u < 1.0):
             continue

@@ -416,3 +416,74 @@ def test_alpha_is_the_mean_of_finite_beta():
     assert n == 3 and a == pytest.approx(0.7, abs=1e-15)
     a, n = O.alpha_from_beta(np.full(4, np.nan))
     assert n == 0 and np.isnan(a)
+
+
+# ----------------------------------------------------------------------------- top-k / nucleus (R9, R10)
+
+def test_topk_threshold_brute_force_and_ties():
+    l = np.array([3.0, 1.0, 3.0, 2.0, -np.inf])
+    assert O.topk_threshold(l, 1) == 3.0 and O.topk_threshold(l, 2) == 3.0      # the tie at 3 is kept
+    assert O.topk_threshold(l, 3) == 2.0 and O.topk_threshold(l, 4) == 1.0
+    assert O.topk_threshold(l, 5) == -np.inf                                       # fewer finite logits
+    rng = np.random.default_rng(8)
+    for _ in range(200):
+        v = rng.normal(0, 3, rng.integers(1, 60))
+        k = int(rng.integers(1, v.size + 2))
+        tau = O.topk_threshold(v, k)
+        kept = np.count_nonzero(v >= tau)
+        assert kept == min(k, v.size)                                # no ties in continuous draws
+        assert np.all(np.sort(v)[::-1][:min(k, v.size)] >= tau)
+
+
+def test_topp_threshold_worked_values():
+    p = np.array([0.5, 0.3, 0.15, 0.05])
+    l = np.log(p)
+    assert O.topp_threshold(l, 1.0, 0.7) == (pytest.approx(np.log(0.3)), False)   # keep {0.5, 0.3}
+    assert O.topp_threshold(l, 1.0, 0.81)[0] == pytest.approx(np.log(0.15))        # keep three
+    assert O.topp_threshold(l, 1.0, 0.5)[0] == pytest.approx(np.log(0.5))          # the top token reaches it
+    tau, flagged = O.topp_threshold(l, 1.0, 0.8)                                   # 0.5 + 0.3 hits 0.8
+    assert flagged
+    assert O.topp_threshold(l, 1.0, 1.0) == (-np.inf, False)
+
+
+def test_topp_threshold_invariants():
+    rng = np.random.default_rng(9)
+    for _ in range(200):
+        l = rng.normal(0, 2, 40)
+        T, top_p = float(rng.uniform(0.5, 2)), float(rng.uniform(0.05, 0.99))
+        tau, flagged = O.topp_threshold(l, T, top_p)
+        p = O.softmax_t(l, T)
+        kept = p[l >= tau].sum()
+        assert kept >= top_p - 1e-12                                 # the kept mass reaches top_p
+        assert kept - p[l == tau].sum() < top_p + 1e-12              # without the boundary token it does not
+
+
+def test_top1_standardised_sampling_is_greedy_verification():
+    """Top-k with k = 1 on both sides turns p and q into one-hot argmax distributions [p1 §2.2], so
+    speculative sampling accepts exactly the guesses greedy verification accepts."""
+    rng = np.random.default_rng(10)
+    B, gamma, V = 40, 4, 30
+    t = rng.normal(0, 2, (B, gamma + 1, V)).astype(np.float32)
+    d = (t[:, :gamma] + rng.normal(0, 1.5, (B, gamma, V))).astype(np.float32)
+    ids = np.argmax(d, axis=2)
+    tthr = np.array([[O.topk_threshold(t[b, i].astype(np.float64), 1) for i in range(gamma + 1)]
+                     for b in range(B)], dtype=np.float32)
+    dthr = np.array([[O.topk_threshold(d[b, i].astype(np.float64), 1) for i in range(gamma)]
+                     for b in range(B)], dtype=np.float32)
+    u = rng.random((B, gamma + 1)).astype(np.float32)
+    s = O.verify_sample(t, d, "f32", ids, None, u, 1.0, tthr=tthr, dthr=dthr)
+    g = O.verify_greedy(t, "f32", ids, None)
+    assert np.array_equal(s["emitted"], g["emitted"]) and np.array_equal(s["n_accepted"], g["n_accepted"])
+
+
+def test_thresholded_sampler_draws_from_the_truncated_softmax():
+    wts = np.array([1.0, 4.0, 0.5, 2.5, 8.0, 0.2])
+    l = np.log(wts)
+    tau = O.topk_threshold(l, 3)                                    # keeps 8, 4, 2.5
+    N = 14500
+    out = O.sample_rows(np.tile(l.astype(np.float32), (N, 1)), "f32", _stratified(N), 1.0,
+                        thr=np.full(N, tau, np.float32))
+    counts = np.bincount(out["tokens"], minlength=wts.size)
+    keep = wts >= 2.5
+    p = np.where(keep, wts, 0) / wts[keep].sum()
+    assert np.all(np.abs(counts - N * p) <= 1.0 + 1e-9)
