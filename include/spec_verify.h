@@ -189,6 +189,44 @@ int spec_sample_rows(const void* logits, int dtype, const float* uniforms, float
                      int R, int V, int32_t* tokens,
                      void* workspace, size_t ws_bytes, void* stream);
 
+/* Top-k and nucleus (top-p) standardisation (paper-graph-ui teardown §2.2
+ * "Standardized Sampling": keep the k largest probabilities, or the shortest
+ * descending prefix whose mass reaches top_p, and renormalise).  Softmax is
+ * increasing in the logit, so the kept set of a row is {x : l(x) >= tau}; these
+ * write tau per row and the *_masked entry points below apply it.
+ *   spec_topk_threshold: tau = the k-th largest logit of the row (k >= 1); ties
+ *     at tau are all kept; tau = -inf when fewer than k logits are finite.
+ *   spec_topp_threshold: tau = the logit of the token at which the descending
+ *     running probability of softmax(l / T) first reaches top_p (0 < top_p <= 1;
+ *     ties at tau kept; -inf for top_p = 1).  Masses are summed in 2^-40 fixed
+ *     point, so a running mass within about 1e-6 of top_p may stop one token
+ *     earlier or later than an exact sum would.
+ *   logits [R, V] dtype (device), thr [R] float32 (device, out).  A row holding
+ *   NaN or +inf (or, for top-p, no finite logit) gets tau = NaN, which the masked
+ *   entry points treat as an invalid row.  One kernel launch, no workspace.
+ *   Returns SPEC_ERR_ARG / SPEC_ERR_DTYPE for bad host arguments. */
+int spec_topk_threshold(const void* logits, int dtype, int R, int V, int k, float* thr, void* stream);
+int spec_topp_threshold(const void* logits, int dtype, float temperature, float top_p, int R, int V, float* thr,
+                        void* stream);
+
+/* spec_verify_sample on standardised distributions: p_i and q_i are the
+ * softmaxes of the logit rows with every logit below the row's threshold set to
+ * -inf (renormalised over the kept tokens), for the accept tests, the residual
+ * and the bonus draw alike.  target_thr [B, gamma+1] and draft_thr [B, gamma]
+ * are float32 device arrays (either may be NULL: no truncation on that side;
+ * -inf in an entry: none for that row).  Other arguments as spec_verify_sample. */
+int spec_verify_sample_masked(const void* target_logits, const void* draft_logits, int dtype,
+                              const int32_t* draft_ids, const int32_t* draft_len, const float* uniforms,
+                              const float* target_thr, const float* draft_thr, float temperature,
+                              int B, int gamma, int V, int32_t* emitted, int32_t* n_accepted,
+                              void* workspace, size_t ws_bytes, void* stream);
+
+/* spec_sample_rows on standardised distributions: thr [R] float32 (device, may be
+ * NULL) as above. */
+int spec_sample_rows_masked(const void* logits, int dtype, const float* uniforms, const float* thr,
+                            float temperature, int R, int V, int32_t* tokens,
+                            void* workspace, size_t ws_bytes, void* stream);
+
 /* Greedy verification: argmax standardisation (paper-graph-ui teardown §2.2;
  * multigrid.ai on sampling temperature).  a_i = argmax_k target[b,i,k], lowest
  * index on ties; guesses are accepted while a_i == draft_ids[b,i]; the emitted

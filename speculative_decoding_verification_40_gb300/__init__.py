@@ -24,7 +24,7 @@ import torch
 __all__ = [
     "SpecVerifyError", "verify_sample", "verify_greedy", "sample_rows", "accept_stats", "check_status", "workspace_size",
     "workspace_for", "plan", "LIB_PATH", "lib", "expected_tokens", "walltime_improvement", "operations_factor",
-    "optimal_gamma", "alpha_mean",
+    "optimal_gamma", "alpha_mean", "topk_threshold", "topp_threshold",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libspecverify.so")
@@ -57,6 +57,14 @@ def _load() -> ctypes.CDLL:
         fn.restype = i32
     L.spec_sample_rows.argtypes = [vp, i32, vp, f32, i32, i32, vp, vp, sz, vp]
     L.spec_sample_rows.restype = i32
+    L.spec_sample_rows_masked.argtypes = [vp, i32, vp, vp, f32, i32, i32, vp, vp, sz, vp]
+    L.spec_sample_rows_masked.restype = i32
+    L.spec_verify_sample_masked.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, f32, i32, i32, i32, vp, vp, vp, sz, vp]
+    L.spec_verify_sample_masked.restype = i32
+    L.spec_topk_threshold.argtypes = [vp, i32, i32, i32, i32, vp, vp]
+    L.spec_topk_threshold.restype = i32
+    L.spec_topp_threshold.argtypes = [vp, i32, f32, f32, i32, i32, vp, vp]
+    L.spec_topp_threshold.restype = i32
     L.spec_verify_greedy.argtypes = [vp, vp, i32, vp, vp, i32, i32, i32, vp, vp, vp, sz, vp]
     L.spec_verify_greedy.restype = i32
     L.spec_accept_stats.argtypes = [vp, vp, i32, vp, vp, f32, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]
@@ -220,7 +228,8 @@ def _common(target, draft, ids, draft_len, gamma_needs_draft=True):
 
 def verify_sample(target: torch.Tensor, draft: torch.Tensor, ids: torch.Tensor, uniforms: torch.Tensor,
                   temperature: float, draft_len: torch.Tensor | None = None, *, emitted=None, n_accepted=None,
-                  workspace: torch.Tensor | None = None, check: bool = False, phase: str = "both"):
+                  workspace: torch.Tensor | None = None, check: bool = False, phase: str = "both",
+                  target_thr: torch.Tensor | None = None, draft_thr: torch.Tensor | None = None):
     """spec_verify_sample: returns (emitted [B, gamma+1] int32, n_accepted [B] int32).
 
     phase="stream" / "draw" calls spec_verify_sample_stream / spec_verify_sample_draw: the two halves
@@ -238,6 +247,22 @@ def verify_sample(target: torch.Tensor, draft: torch.Tensor, ids: torch.Tensor, 
     _cuda(emitted, "emitted", torch.int32, (B, G + 1))
     _cuda(n_accepted, "n_accepted", torch.int32, (B,))
     ws = workspace if workspace is not None else workspace_for(dev, workspace_size(B, G, V, target.dtype))
+    if target_thr is not None or draft_thr is not None:  # spec_verify_sample_masked
+        if phase != "both":
+            raise ValueError("standardisation thresholds go with phase='both'")
+        if target_thr is not None:
+            _cuda(target_thr, "target_thr", torch.float32, (B, G + 1))
+        if draft_thr is not None and G > 0:
+            _cuda(draft_thr, "draft_thr", torch.float32, (B, G))
+        code = lib.spec_verify_sample_masked(_p(target), _p(draft) if G > 0 else None, _dtype_code(target),
+                                             _p(ids) if G > 0 else None, _p(draft_len), _p(uniforms),
+                                             _p(target_thr), _p(draft_thr) if G > 0 else None, float(temperature),
+                                             B, G, V, _p(emitted), _p(n_accepted), _p(ws), ws.numel(),
+                                             _stream(dev))
+        _raise(code, "spec_verify_sample_masked")
+        if check:
+            check_status(ws)
+        return emitted, n_accepted
     fn = {"both": lib.spec_verify_sample, "stream": lib.spec_verify_sample_stream,
           "draw": lib.spec_verify_sample_draw, "early_exit": lib.spec_verify_sample_early_exit}[phase]
     code = fn(_p(target), _p(draft) if G > 0 else None, _dtype_code(target), _p(ids) if G > 0 else None,
@@ -249,9 +274,10 @@ def verify_sample(target: torch.Tensor, draft: torch.Tensor, ids: torch.Tensor, 
     return emitted, n_accepted
 
 
-def sample_rows(logits: torch.Tensor, uniforms: torch.Tensor, temperature: float, *, tokens=None,
+def sample_rows(logits: torch.Tensor, uniforms: torch.Tensor, temperature: float, *, thr=None, tokens=None,
                 workspace: torch.Tensor | None = None, check: bool = False) -> torch.Tensor:
-    """spec_sample_rows: logits [R, V], uniforms [R] float32; returns tokens [R] int32."""
+    """spec_sample_rows (spec_sample_rows_masked with thr [R] float32): logits [R, V], uniforms [R]
+    float32; returns tokens [R] int32."""
     if logits.dim() != 2:
         raise ValueError("logits must be [R, V]")
     R, V = logits.shape
@@ -262,12 +288,39 @@ def sample_rows(logits: torch.Tensor, uniforms: torch.Tensor, temperature: float
         tokens = torch.empty(R, dtype=torch.int32, device=dev)
     _cuda(tokens, "tokens", torch.int32, (R,))
     ws = workspace if workspace is not None else workspace_for(dev, workspace_size(R, 0, V, logits.dtype))
-    code = lib.spec_sample_rows(_p(logits), _dtype_code(logits), _p(uniforms), float(temperature), R, V,
-                                _p(tokens), _p(ws), ws.numel(), _stream(dev))
+    if thr is None:
+        code = lib.spec_sample_rows(_p(logits), _dtype_code(logits), _p(uniforms), float(temperature), R, V,
+                                    _p(tokens), _p(ws), ws.numel(), _stream(dev))
+    else:
+        _cuda(thr, "thr", torch.float32, (R,))
+        code = lib.spec_sample_rows_masked(_p(logits), _dtype_code(logits), _p(uniforms), _p(thr),
+                                           float(temperature), R, V, _p(tokens), _p(ws), ws.numel(), _stream(dev))
     _raise(code, "spec_sample_rows")
     if check:
         check_status(ws)
     return tokens
+
+
+def topk_threshold(logits: torch.Tensor, k: int) -> torch.Tensor:
+    """spec_topk_threshold: logits [..., V]; returns the per-row threshold (float32, shape [...])."""
+    V = logits.shape[-1]
+    _cuda(logits, "logits")
+    R = logits.numel() // V
+    thr = torch.empty(logits.shape[:-1], dtype=torch.float32, device=logits.device)
+    _raise(lib.spec_topk_threshold(_p(logits), _dtype_code(logits), R, V, int(k), _p(thr), _stream(logits.device)),
+           "spec_topk_threshold")
+    return thr
+
+
+def topp_threshold(logits: torch.Tensor, temperature: float, top_p: float) -> torch.Tensor:
+    """spec_topp_threshold: logits [..., V]; returns the per-row threshold (float32, shape [...])."""
+    V = logits.shape[-1]
+    _cuda(logits, "logits")
+    R = logits.numel() // V
+    thr = torch.empty(logits.shape[:-1], dtype=torch.float32, device=logits.device)
+    _raise(lib.spec_topp_threshold(_p(logits), _dtype_code(logits), float(temperature), float(top_p), R, V, _p(thr),
+                                   _stream(logits.device)), "spec_topp_threshold")
+    return thr
 
 
 def verify_greedy(target: torch.Tensor, ids: torch.Tensor, draft_len: torch.Tensor | None = None,

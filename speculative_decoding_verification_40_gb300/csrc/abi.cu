@@ -239,7 +239,7 @@ int run_verify(const void* target, const void* draft, int dtype, const int32_t* 
                const float* uniforms, float temperature, int B, int gamma, int V, int32_t* emitted,
                int32_t* n_accepted, float* beta, float* p_draft, float* q_draft, float* accept_prob,
                float* resid, void* workspace, size_t ws_bytes, void* stream, bool stats, int phases = 3,
-               bool early_exit = false) {
+               bool early_exit = false, const float* tthr = nullptr, const float* dthr = nullptr) {
   int st = check_common(dtype, B, gamma, V, workspace, ws_bytes);
   if (st != SPEC_OK) return st;
   if (!(std::isfinite(temperature) && temperature > 0.f)) return SPEC_ERR_ARG;
@@ -257,6 +257,8 @@ int run_verify(const void* target, const void* draft, int dtype, const int32_t* 
     p.ids = ids;
     p.draft_len = draft_len;
     p.uniforms = uniforms;
+    p.tthr = tthr;
+    p.dthr = gamma > 0 ? dthr : nullptr;
     p.scale = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
     p.B = B;
     p.G = gamma;
@@ -359,8 +361,53 @@ int spec_verify_sample_early_exit(const void* target_logits, const void* draft_l
                     false, 3, true);
 }
 
+int spec_verify_sample_masked(const void* target_logits, const void* draft_logits, int dtype,
+                              const int32_t* draft_ids, const int32_t* draft_len, const float* uniforms,
+                              const float* target_thr, const float* draft_thr, float temperature, int B, int gamma,
+                              int V, int32_t* emitted, int32_t* n_accepted, void* workspace, size_t ws_bytes,
+                              void* stream) {
+  return run_verify(target_logits, draft_logits, dtype, draft_ids, draft_len, uniforms, temperature, B, gamma, V,
+                    emitted, n_accepted, nullptr, nullptr, nullptr, nullptr, nullptr, workspace, ws_bytes, stream,
+                    false, 3, false, target_thr, draft_thr);
+}
+
+int spec_topk_threshold(const void* logits, int dtype, int R, int V, int k, float* thr, void* stream) {
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
+  if (R < 0 || V < 1 || V > SPEC_MAX_VOCAB || k < 1) return SPEC_ERR_ARG;
+  if (R == 0) return SPEC_OK;
+  if (logits == nullptr || thr == nullptr) return SPEC_ERR_ARG;
+  const int esz = dtype == SPEC_F32 ? 4 : 2;
+  return launch_status(specv::topk_threshold_launch(logits, dtype, R, V, k, rows_aligned(logits, V, esz) ? 1 : 0,
+                                                    thr, static_cast<cudaStream_t>(stream)));
+}
+
+int spec_topp_threshold(const void* logits, int dtype, float temperature, float top_p, int R, int V, float* thr,
+                        void* stream) {
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
+  if (R < 0 || V < 1 || V > SPEC_MAX_VOCAB) return SPEC_ERR_ARG;
+  if (!(std::isfinite(temperature) && temperature > 0.f) || !(top_p > 0.f && top_p <= 1.f)) return SPEC_ERR_ARG;
+  if (R == 0) return SPEC_OK;
+  if (logits == nullptr || thr == nullptr) return SPEC_ERR_ARG;
+  const int esz = dtype == SPEC_F32 ? 4 : 2;
+  const float scale = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+  return launch_status(specv::topp_threshold_launch(logits, dtype, R, V, scale, top_p,
+                                                    rows_aligned(logits, V, esz) ? 1 : 0, thr,
+                                                    static_cast<cudaStream_t>(stream)));
+}
+
+int spec_sample_rows_masked(const void* logits, int dtype, const float* uniforms, const float* thr,
+                            float temperature, int R, int V, int32_t* tokens, void* workspace, size_t ws_bytes,
+                            void* stream);
+
 int spec_sample_rows(const void* logits, int dtype, const float* uniforms, float temperature, int R, int V,
                      int32_t* tokens, void* workspace, size_t ws_bytes, void* stream) {
+  return spec_sample_rows_masked(logits, dtype, uniforms, nullptr, temperature, R, V, tokens, workspace, ws_bytes,
+                                 stream);
+}
+
+int spec_sample_rows_masked(const void* logits, int dtype, const float* uniforms, const float* thr,
+                            float temperature, int R, int V, int32_t* tokens, void* workspace, size_t ws_bytes,
+                            void* stream) {
   int st = check_common(dtype, R, 0, V, workspace, ws_bytes);
   if (st != SPEC_OK) return st;
   if (!(std::isfinite(temperature) && temperature > 0.f)) return SPEC_ERR_ARG;
@@ -370,6 +417,7 @@ int spec_sample_rows(const void* logits, int dtype, const float* uniforms, float
   specv::SampleParams p = {};
   p.target = logits;
   p.uniforms = uniforms;
+  p.tthr = thr;
   p.scale = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
   p.B = R;
   p.G = 0;

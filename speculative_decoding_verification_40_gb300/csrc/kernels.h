@@ -44,6 +44,8 @@ struct SampleParams {
   const int32_t* ids;        // [B, G]
   const int32_t* draft_len;  // [B] or nullptr
   const float* uniforms;     // [B, G+1]
+  const float* tthr;         // [B, G+1] standardisation thresholds of the target rows, or nullptr
+  const float* dthr;         // [B, G] standardisation thresholds of the draft rows, or nullptr
   float scale;               // log2(e) / T
   int B, G, V;
   int slice;                 // vocabulary elements per work item (a multiple of 32 x elements per 16 bytes)
@@ -67,6 +69,11 @@ cudaError_t sample_launch(const SampleParams& p, int dtype, int phases, cudaStre
 cudaError_t sample_early_exit_launch(SampleParams p, int dtype, cudaStream_t stream);
 // stream kernel (gamma = 0) then one sampling CTA per row; emitted is the [B] token output
 cudaError_t rows_sample_launch(const SampleParams& p, int dtype, cudaStream_t stream);
+// one CTA per row: the logit threshold of top-k / nucleus standardisation
+cudaError_t topk_threshold_launch(const void* logits, int dtype, int R, int V, int k, int vec, float* thr,
+                                  cudaStream_t stream);
+cudaError_t topp_threshold_launch(const void* logits, int dtype, int R, int V, float scale, float top_p, int vec,
+                                  float* thr, cudaStream_t stream);
 cudaError_t greedy_launch(const GreedyParams& p, int dtype, cudaStream_t stream);
 
 }  // namespace specv

@@ -47,6 +47,7 @@ struct RowState {
   int n, flags;
   uint32_t err;
   float mp, ip, mq, iq;
+  float tt, dt;  // standardisation thresholds of the drawn target / draft row (-inf: none)
 };
 
 // Weights of one lane's kV elements starting at `base` of the drawn row(s): p, and w = max(0, p - q)
@@ -70,8 +71,8 @@ __device__ __forceinline__ void seg_weights(const T* tr, const T* dr, bool resid
   }
 #pragma unroll
   for (int j = 0; j < kV; ++j) {
-    p[j] = fast_exp2((lt[j] - st.mp) * sc) * st.ip;
-    w[j] = resid ? fmaxf(p[j] - fast_exp2((ld[j] - st.mq) * sc) * st.iq, 0.f) : p[j];
+    p[j] = fast_exp2((masked(lt[j], st.tt) - st.mp) * sc) * st.ip;
+    w[j] = resid ? fmaxf(p[j] - fast_exp2((masked(ld[j], st.dt) - st.mq) * sc) * st.iq, 0.f) : p[j];
   }
 }
 
@@ -183,9 +184,12 @@ __device__ RowState decide_row(const SampleParams& a, int b, int gb, DrawSmem& s
     st.flags = n < gb ? kRowResid : 0;
     st.mp = sm.mp[n];
     st.ip = 1.f / sm.sp[n];
+    st.tt = a.tthr ? __ldg(a.tthr + (size_t)b * G1 + n) : -INFINITY;
+    st.dt = -INFINITY;
     if (n < gb) {
       st.mq = sm.mq[n];
       st.iq = 1.f / sm.sq[n];
+      if (a.dthr) st.dt = __ldg(a.dthr + (size_t)b * a.G + n);
     }
   }
   return st;
@@ -362,10 +366,10 @@ __device__ void resolve_row(const SampleParams& a, int b, int gb, const RowState
 // Online normalisers (m, S) of n logits of one row (and of a second row when has_q), this thread's
 // share: 16-byte vectors when vec, in groups of U per row in flight, then a scalar tail.  raw tracks the
 // NaN-propagating maximum of the raw logits (NaN / +inf detection).
-template <typename T>
+template <typename T, bool kMask>
 __device__ __forceinline__ void slice_normalisers(const T* __restrict__ tp, const T* __restrict__ dp, bool has_q,
-                                                  int n, bool vec, float sc, float& mp, float& sp, float& rp,
-                                                  float& mq, float& sq, float& rq) {
+                                                  int n, bool vec, float sc, float tt, float dt, float& mp,
+                                                  float& sp, float& rp, float& mq, float& sq, float& rq) {
   constexpr int kV = Elems<T>::kVec;
   constexpr int U = 4;
   const int tid = threadIdx.x;
@@ -382,35 +386,35 @@ __device__ __forceinline__ void slice_normalisers(const T* __restrict__ tp, cons
         for (int u = 0; u < U; ++u) r0[u] = ldg_stream(t4 + v + u * kST);
 #pragma unroll
         for (int u = 0; u < U; ++u) r1[u] = ldg_stream(d4 + v + u * kST);
-        online_group<T, U>(mp, sp, rp, r0, sc);
-        online_group<T, U>(mq, sq, rq, r1, sc);
+        online_group<T, U, kMask>(mp, sp, rp, r0, sc, tt);
+        online_group<T, U, kMask>(mq, sq, rq, r1, sc, dt);
       }
       for (; v < nv; v += kST) {
         const uint4 r0[1] = {ldg_stream(t4 + v)};
         const uint4 r1[1] = {ldg_stream(d4 + v)};
-        online_group<T, 1>(mp, sp, rp, r0, sc);
-        online_group<T, 1>(mq, sq, rq, r1, sc);
+        online_group<T, 1, kMask>(mp, sp, rp, r0, sc, tt);
+        online_group<T, 1, kMask>(mq, sq, rq, r1, sc, dt);
       }
     } else {
       for (; v + (U - 1) * kST < nv; v += U * kST) {
         uint4 r0[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) r0[u] = ldg_stream(t4 + v + u * kST);
-        online_group<T, U>(mp, sp, rp, r0, sc);
+        online_group<T, U, kMask>(mp, sp, rp, r0, sc, tt);
       }
       for (; v < nv; v += kST) {
         const uint4 r0[1] = {ldg_stream(t4 + v)};
-        online_group<T, 1>(mp, sp, rp, r0, sc);
+        online_group<T, 1, kMask>(mp, sp, rp, r0, sc, tt);
       }
     }
     done = nv * kV;
   }
   for (int k = done + tid; k < n; k += kST) {
     float f[1] = {Elems<T>::one(tp, k)};
-    online<1>(mp, sp, rp, f, sc);
+    online<1, kMask>(mp, sp, rp, f, sc, tt);
     if (has_q) {
       f[0] = Elems<T>::one(dp, k);
-      online<1>(mq, sq, rq, f, sc);
+      online<1, kMask>(mq, sq, rq, f, sc, dt);
     }
   }
 }
@@ -449,7 +453,7 @@ __device__ __forceinline__ void block_normalisers(float mp, float sp, float rp, 
   }
 }
 
-template <typename T>
+template <typename T, bool kMask>
 __global__ void __launch_bounds__(kStreamThreads, 4) verify_stream_kernel(const SampleParams a) {
   __shared__ float red[4][kSW];
   __shared__ float rawr[kSW];
@@ -486,7 +490,9 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_stream_kernel(const 
 
   float mp = -INFINITY, sp = 0.f, rp = -INFINITY;
   float mq = -INFINITY, sq = 0.f, rq = -INFINITY;
-  slice_normalisers<T>(tp, dp, has_q, n, a.vec != 0, sc, mp, sp, rp, mq, sq, rq);
+  const float tt = kMask && a.tthr ? __ldg(a.tthr + pos) : -INFINITY;
+  const float dt = kMask && has_q && a.dthr ? __ldg(a.dthr + (size_t)b * a.G + i) : -INFINITY;
+  slice_normalisers<T, kMask>(tp, dp, has_q, n, a.vec != 0, sc, tt, dt, mp, sp, rp, mq, sq, rq);
   float4 nrm;
   float raw;
   block_normalisers(mp, sp, rp, mq, sq, rq, sc, red, rawr, nrm, raw);
@@ -494,7 +500,7 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_stream_kernel(const 
     const int x = __ldg(a.ids + (size_t)b * a.G + i);
     if (x >= lo && x < lo + n)
       reinterpret_cast<float2*>(a.ws.xl)[(size_t)b * a.G + i] =
-          make_float2(Elems<T>::one(tp, x - lo), Elems<T>::one(dp, x - lo));
+          make_float2(masked(Elems<T>::one(tp, x - lo), tt), masked(Elems<T>::one(dp, x - lo), dt));
   }
   if (tid == 0) {
     const bool bad = !(raw < INFINITY);  // NaN or +inf in this slice
@@ -575,8 +581,8 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_draw_kernel(const Sa
           float sw = 0.f, spp = 0.f;
 #pragma unroll
           for (int j = 0; j < kV; ++j) {
-            const float p = fast_exp2((lt[j] - st.mp) * sc) * st.ip;
-            const float w = resid ? fmaxf(p - fast_exp2((ld[j] - st.mq) * sc) * st.iq, 0.f) : p;
+            const float p = fast_exp2((masked(lt[j], st.tt) - st.mp) * sc) * st.ip;
+            const float w = resid ? fmaxf(p - fast_exp2((masked(ld[j], st.dt) - st.mq) * sc) * st.iq, 0.f) : p;
             sw += w;
             spp += p;
           }
@@ -646,8 +652,8 @@ cudaError_t sample_early_exit_launch(SampleParams p, int dtype, cudaStream_t str
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = i > 0 ? 1 : 0;  // each position's launch overlaps the previous one's tail
-    const cudaError_t e = dtype == 0 ? cudaLaunchKernelEx(&cfg, verify_stream_kernel<float>, p)
-                                     : cudaLaunchKernelEx(&cfg, verify_stream_kernel<__nv_bfloat16>, p);
+    const cudaError_t e = dtype == 0 ? cudaLaunchKernelEx(&cfg, verify_stream_kernel<float, false>, p)
+                                     : cudaLaunchKernelEx(&cfg, verify_stream_kernel<__nv_bfloat16, false>, p);
     if (e != cudaSuccess) return e;
   }
   p.step = 0;
@@ -665,7 +671,7 @@ cudaError_t sample_early_exit_launch(SampleParams p, int dtype, cudaStream_t str
 namespace {
 
 template <typename T>
-__device__ __forceinline__ void row_weights(const T* row, bool vec, int base, int n, float sc, float nm,
+__device__ __forceinline__ void row_weights(const T* row, bool vec, int base, int n, float sc, float nm, float thr,
                                             float (&w)[Elems<T>::kVec]) {
   constexpr int kV = Elems<T>::kVec;
   float f[kV];
@@ -676,7 +682,7 @@ __device__ __forceinline__ void row_weights(const T* row, bool vec, int base, in
     for (int j = 0; j < kV; ++j) f[j] = base + j < n ? Elems<T>::one(row, base + j) : -INFINITY;
   }
 #pragma unroll
-  for (int j = 0; j < kV; ++j) w[j] = fast_exp2(fmaf(f[j], sc, nm));
+  for (int j = 0; j < kV; ++j) w[j] = fast_exp2(fmaf(masked(f[j], thr), sc, nm));
 }
 
 }  // namespace
@@ -686,7 +692,7 @@ __device__ __forceinline__ void row_weights(const T* row, bool vec, int base, in
 // If rounding leaves t beyond the slice's mass the draw is the slice's last token of positive weight.
 // Returns the token's index in the slice in warp 0 (-1 elsewhere, or if the slice has no positive weight).
 template <typename T>
-__device__ int draw_in_slice(const T* srow, int n, bool vec, float sc, float nm, float t, float* cm) {
+__device__ int draw_in_slice(const T* srow, int n, bool vec, float sc, float nm, float thr, float t, float* cm) {
   constexpr int kV = Elems<T>::kVec;
   constexpr int kCpc = kR * 32 * kV;  // elements per chunk: kR vectors per lane
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -696,7 +702,7 @@ __device__ int draw_in_slice(const T* srow, int n, bool vec, float sc, float nm,
 #pragma unroll
     for (int r = 0; r < kR; ++r) {
       float w[kV];
-      row_weights<T>(srow, vec, c * kCpc + (r * 32 + lane) * kV, n, sc, nm, w);
+      row_weights<T>(srow, vec, c * kCpc + (r * 32 + lane) * kV, n, sc, nm, thr, w);
 #pragma unroll
       for (int j = 0; j < kV; ++j) acc += w[j];
     }
@@ -730,7 +736,7 @@ __device__ int draw_in_slice(const T* srow, int n, bool vec, float sc, float nm,
     for (int r = 0; r < kR && token < 0; ++r) {
       const int base = chunk * kCpc + (r * 32 + lane) * kV;
       float w[kV];
-      row_weights<T>(srow, vec, base, n, sc, nm, w);
+      row_weights<T>(srow, vec, base, n, sc, nm, thr, w);
       float ls = 0.f;
 #pragma unroll
       for (int j = 0; j < kV; ++j) ls += w[j];
@@ -768,9 +774,9 @@ __device__ int draw_in_slice(const T* srow, int n, bool vec, float sc, float nm,
 
 // Online normaliser (m, S) of a contiguous segment of n logits, merged over the warp (every lane gets
 // it), and the NaN-propagating raw maximum.  16-byte loads when vec, four in flight per lane.
-template <typename T>
-__device__ __forceinline__ void warp_segment(const T* __restrict__ seg, int n, bool vec, float sc, float& m,
-                                             float& sm, float& raw) {
+template <typename T, bool kMask>
+__device__ __forceinline__ void warp_segment(const T* __restrict__ seg, int n, bool vec, float sc, float thr,
+                                             float& m, float& sm, float& raw) {
   constexpr int kV = Elems<T>::kVec;
   constexpr int U = 4;
   const int lane = threadIdx.x & 31;
@@ -786,16 +792,16 @@ __device__ __forceinline__ void warp_segment(const T* __restrict__ seg, int n, b
         uint4 r[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) r[u] = ldg_stream(v4 + j + u * 32);
-        online_group<T, U>(m, sm, raw, r, sc);
+        online_group<T, U, kMask>(m, sm, raw, r, sc, thr);
       }
       for (; j < nv; j += 32) {
         const uint4 r[1] = {ldg_stream(v4 + j)};
-        online_group<T, 1>(m, sm, raw, r, sc);
+        online_group<T, 1, kMask>(m, sm, raw, r, sc, thr);
       }
     } else {
       for (int k = lane; k < n; k += 32) {
         float f[1] = {Elems<T>::one(seg, k)};
-        online<1>(m, sm, raw, f, sc);
+        online<1, kMask>(m, sm, raw, f, sc, thr);
       }
     }
   }
@@ -817,7 +823,7 @@ __host__ __device__ __forceinline__ int segment_len(int L) {
 // the row once for its online normalisers (m_w, S_w); thread 0 combines the eight segments in order,
 // picks the segment holding u * Z from their masses S_w 2^((m_w - M) log2(e)/T), and the CTA draws
 // inside that segment only (its second read, an eighth of the row, hits L2).
-template <typename T>
+template <typename T, bool kMask>
 __global__ void __launch_bounds__(kST) sample_rows_fused_kernel(const SampleParams a) {
   __shared__ float segm[kSW], segs[kSW], segr[kSW];
   __shared__ float cm[kMaxChunksPerSlice];
@@ -830,10 +836,11 @@ __global__ void __launch_bounds__(kST) sample_rows_fused_kernel(const SamplePara
   const T* row = reinterpret_cast<const T*>(a.target) + (size_t)b * V;
   const bool vec = a.vec != 0;
   const int segE = segment_len<T>(V);
+  const float thr = kMask && a.tthr ? __ldg(a.tthr + b) : -INFINITY;
   {
     const int lo = warp * segE;
     float m, sm, raw;
-    warp_segment<T>(row + lo, min(V, lo + segE) - lo, vec, sc, m, sm, raw);
+    warp_segment<T, kMask>(row + lo, min(V, lo + segE) - lo, vec, sc, thr, m, sm, raw);
     if (lane == 0) {
       segm[warp] = m;
       segs[warp] = sm;
@@ -882,14 +889,14 @@ __global__ void __launch_bounds__(kST) sample_rows_fused_kernel(const SamplePara
   }
   const int lo = sh_w * segE;
   const int n = min(V, lo + segE) - lo;
-  const int tok = draw_in_slice<T>(row + lo, n, vec, sc, -sh_m * sc, sh_t, cm);
+  const int tok = draw_in_slice<T>(row + lo, n, vec, sc, -sh_m * sc, thr, sh_t, cm);
   if (tid == 0) a.emitted[b] = tok >= 0 ? lo + tok : -1;
 }
 
 // Rows longer than one slice, pass 1: one CTA per (row b, slice s); warp w writes the normaliser of
 // its segment of the slice, (m, S) with m = NaN if the segment holds NaN or +inf, to the workspace's
 // per-row segment list [b][s * 8 + w].
-template <typename T>
+template <typename T, bool kMask>
 __global__ void __launch_bounds__(kST, 4) sample_stream_kernel(const SampleParams a) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   asm volatile("griddepcontrol.launch_dependents;");
@@ -900,8 +907,9 @@ __global__ void __launch_bounds__(kST, 4) sample_stream_kernel(const SampleParam
   const int lo = s * a.slice + warp * segE;
   const int hi = min(a.V, min(s * a.slice + a.slice, lo + segE));
   float m, sm, raw;
-  warp_segment<T>(reinterpret_cast<const T*>(a.target) + (size_t)b * a.V + lo, hi - lo, a.vec != 0, a.scale, m, sm,
-                  raw);
+  const float thr = kMask && a.tthr ? __ldg(a.tthr + b) : -INFINITY;
+  warp_segment<T, kMask>(reinterpret_cast<const T*>(a.target) + (size_t)b * a.V + lo, hi - lo, a.vec != 0, a.scale,
+                         thr, m, sm, raw);
   if (lane == 0)
     reinterpret_cast<float2*>(a.ws.dch)[(size_t)b * chunks_per_row(a.V) + s * kSW + warp] =
         make_float2(raw < INFINITY ? m : NAN, sm);
@@ -969,7 +977,8 @@ __global__ void __launch_bounds__(kST) sample_rows_kernel(const SampleParams a) 
   const int lo = s * a.slice + w * segE;
   const int n = min(a.V, min(s * a.slice + a.slice, lo + segE)) - lo;
   const T* srow = reinterpret_cast<const T*>(a.target) + (size_t)b * a.V + lo;
-  const int tok = draw_in_slice<T>(srow, n, a.vec != 0, sc, -M * sc, beyond ? INFINITY : sh_t, cm);
+  const float thr = a.tthr ? __ldg(a.tthr + b) : -INFINITY;
+  const int tok = draw_in_slice<T>(srow, n, a.vec != 0, sc, -M * sc, thr, beyond ? INFINITY : sh_t, cm);
   if (tid == 0) a.emitted[b] = tok >= 0 ? lo + tok : -1;
 }
 
@@ -987,41 +996,43 @@ static cudaError_t launch_rows(const SampleParams& p, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, sample_rows_kernel<T>, p);
 }
 
-cudaError_t rows_sample_launch(const SampleParams& p, int dtype, cudaStream_t stream) {
+template <typename T, bool kMask>
+static cudaError_t rows_sample_launch_t(const SampleParams& p, cudaStream_t stream) {
   const dim3 block(kStreamThreads);
-  const dim3 g1(static_cast<unsigned>((long long)p.B * p.nslices));
-  cudaError_t e;
   if (p.nslices == 1) {
-    if (dtype == 0)
-      sample_rows_fused_kernel<float><<<dim3(static_cast<unsigned>(p.B)), block, 0, stream>>>(p);
-    else
-      sample_rows_fused_kernel<__nv_bfloat16><<<dim3(static_cast<unsigned>(p.B)), block, 0, stream>>>(p);
+    sample_rows_fused_kernel<T, kMask><<<dim3(static_cast<unsigned>(p.B)), block, 0, stream>>>(p);
     return cudaGetLastError();
   }
-  if (dtype == 0) {
-    sample_stream_kernel<float><<<g1, block, 0, stream>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    return launch_rows<float>(p, stream);
+  sample_stream_kernel<T, kMask><<<dim3(static_cast<unsigned>((long long)p.B * p.nslices)), block, 0, stream>>>(p);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_rows<T>(p, stream);
+}
+
+cudaError_t rows_sample_launch(const SampleParams& p, int dtype, cudaStream_t stream) {
+  const bool mask = p.tthr != nullptr;
+  if (dtype == 0) return mask ? rows_sample_launch_t<float, true>(p, stream) : rows_sample_launch_t<float, false>(p, stream);
+  return mask ? rows_sample_launch_t<__nv_bfloat16, true>(p, stream)
+              : rows_sample_launch_t<__nv_bfloat16, false>(p, stream);
+}
+
+template <typename T, bool kMask>
+static cudaError_t sample_launch_t(const SampleParams& p, int phases, cudaStream_t stream) {
+  const dim3 block(kStreamThreads);
+  const dim3 g1(static_cast<unsigned>((long long)p.B * (p.G + 1) * p.nslices));
+  if (phases & 1) {
+    verify_stream_kernel<T, kMask><<<g1, block, 0, stream>>>(p);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
   }
-  sample_stream_kernel<__nv_bfloat16><<<g1, block, 0, stream>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  return launch_rows<__nv_bfloat16>(p, stream);
+  return (phases & 2) ? launch_draw<T>(p, stream) : cudaSuccess;
 }
 
 cudaError_t sample_launch(const SampleParams& p, int dtype, int phases, cudaStream_t stream) {
-  const dim3 block(kStreamThreads);
-  const dim3 g1(static_cast<unsigned>((long long)p.B * (p.G + 1) * p.nslices));
-  cudaError_t e = cudaSuccess;
-  if (dtype == 0) {
-    if (phases & 1) verify_stream_kernel<float><<<g1, block, 0, stream>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if (phases & 2) e = launch_draw<float>(p, stream);
-  } else {
-    if (phases & 1) verify_stream_kernel<__nv_bfloat16><<<g1, block, 0, stream>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if (phases & 2) e = launch_draw<__nv_bfloat16>(p, stream);
-  }
-  return e;
+  const bool mask = p.tthr != nullptr || p.dthr != nullptr;
+  if (dtype == 0) return mask ? sample_launch_t<float, true>(p, phases, stream) : sample_launch_t<float, false>(p, phases, stream);
+  return mask ? sample_launch_t<__nv_bfloat16, true>(p, phases, stream)
+              : sample_launch_t<__nv_bfloat16, false>(p, phases, stream);
 }
 
 }  // namespace specv

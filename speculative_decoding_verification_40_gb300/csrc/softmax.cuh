@@ -14,8 +14,13 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 // Online normaliser update with a group of raw logits.
-template <int kCnt>
-__device__ __forceinline__ void online(float& m, float& s, float& raw, const float* f, float sc) {
+// With kMask, logits below thr count as -inf in the sum (a standardised row: top-k / nucleus); the
+// running max and the raw max still see every logit (the max is always kept, so it is a valid shift).
+__device__ __forceinline__ float masked(float f, float thr) { return f < thr ? -INFINITY : f; }
+
+template <int kCnt, bool kMask = false>
+__device__ __forceinline__ void online(float& m, float& s, float& raw, const float* f, float sc,
+                                       float thr = -INFINITY) {
   float vm = f[0];
 #pragma unroll
   for (int j = 1; j < kCnt; ++j) vm = max_nan(vm, f[j]);
@@ -27,7 +32,7 @@ __device__ __forceinline__ void online(float& m, float& s, float& raw, const flo
     }
     float acc = 0.f;
 #pragma unroll
-    for (int j = 0; j < kCnt; ++j) acc += fast_exp2((f[j] - m) * sc);
+    for (int j = 0; j < kCnt; ++j) acc += fast_exp2(((kMask ? masked(f[j], thr) : f[j]) - m) * sc);
     s += acc;
   }
 }
@@ -79,8 +84,9 @@ struct GroupMax<__nv_bfloat16, U> {
 
 // Online normaliser update with U 16-byte vectors of raw logits: one max and one rescale per group,
 // then 2^((l - m) log2(e)/T) per element as a single FFMA and a hardware exp2.
-template <typename T, int U>
-__device__ __forceinline__ void online_group(float& m, float& s, float& raw, const uint4 (&r)[U], float sc) {
+template <typename T, int U, bool kMask = false>
+__device__ __forceinline__ void online_group(float& m, float& s, float& raw, const uint4 (&r)[U], float sc,
+                                             float thr = -INFINITY) {
   constexpr int kV = Elems<T>::kVec;
   const float vm = GroupMax<T, U>::get(r);
   raw = max_nan(raw, vm);
@@ -97,8 +103,8 @@ __device__ __forceinline__ void online_group(float& m, float& s, float& raw, con
       Elems<T>::widen(r[u], f);
 #pragma unroll
       for (int j = 0; j < kV; j += 2) {
-        a0 += fast_exp2(fmaf(f[j], sc, nc));
-        a1 += fast_exp2(fmaf(f[j + 1], sc, nc));
+        a0 += fast_exp2(fmaf(kMask ? masked(f[j], thr) : f[j], sc, nc));
+        a1 += fast_exp2(fmaf(kMask ? masked(f[j + 1], thr) : f[j + 1], sc, nc));
       }
     }
     s += a0 + a1;
