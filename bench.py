@@ -331,6 +331,17 @@ def run_ours(a, rank, world, dist):
     n_b = na.long()
     g_b = w.draft_len.long() if w.draft_len is not None else torch.full_like(n_b, w.gamma)
     early_rows = int(((n_b + 1) + torch.where(n_b < g_b, n_b + 1, g_b)).sum())
+    # top-k / nucleus standardisation: per-row thresholds of the target and draft logits, then verification
+    # on the standardised distributions (spec_verify_sample_masked)
+    topk_ms = time_device(lambda: (S.topk_threshold(w.target, 50), S.topk_threshold(w.draft, 50)),
+                          max(10, a.steps // 4), 3, stream)
+    topp_ms = time_device(lambda: (S.topp_threshold(w.target, w.T, 0.9), S.topp_threshold(w.draft, w.T, 0.9)),
+                          max(10, a.steps // 4), 3, stream)
+    tthr, dthr = S.topp_threshold(w.target, w.T, 0.9), S.topp_threshold(w.draft, w.T, 0.9)
+    masked_ms = time_device(lambda: S.verify_sample(w.target, w.draft, w.ids, w.uniforms, w.T, w.draft_len,
+                                                    emitted=em, n_accepted=na, workspace=ws, target_thr=tthr,
+                                                    draft_thr=dthr), max(10, a.steps), 3, stream)
+    S.check_status(ws, raise_on_error=False)        # padded draft rows (NaN) have NaN thresholds: never read
     s_logits, s_u = W.sampler_rows(w)               # the draft-side sampler over every draft row
     sampler_ms = time_device(lambda: S.sample_rows(s_logits, s_u, w.T), max(10, a.steps), 3, stream)
     esz = 4 if w.dtype == "f32" else 2
@@ -379,6 +390,9 @@ def run_ours(a, rank, world, dist):
                      "greedy_GB_per_s": greedy_bytes / (greedy_ms * 1e-3) / 1e9,
                      "stats_ms_per_call": stats_ms,
                      "stats_GB_per_s": stats_bytes / (stats_ms * 1e-3) / 1e9,
+                     "topk50_thresholds_ms": topk_ms, "topp09_thresholds_ms": topp_ms,
+                     "thresholds_GB_per_s": (w.B * (2 * w.gamma + 1)) * w.V * esz / (topp_ms * 1e-3) / 1e9,
+                     "masked_verify_ms_per_call": masked_ms,
                      "early_exit_ms_per_call": early_ms,
                      "early_exit_rows_read": early_rows, "all_positions_rows_read": w.B + 2 * pos,
                      "early_exit_GB_per_s": early_rows * w.V * esz / (early_ms * 1e-3) / 1e9,
