@@ -243,7 +243,7 @@ def run_ours(a, rank, world, dist):
     import speculative_decoding_verification_40_gb300 as S
     dev = torch.device("cuda", torch.cuda.current_device())
     k = int(a.workload.lstrip("c"))
-    w = W.make(k, device=dev)
+    w = W.make(k, device=dev, B=a.batch or None)
     stream = torch.cuda.current_stream(dev)
     pos = w.positions()
     nbytes = w.read_once_bytes()
@@ -443,6 +443,9 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-also", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="rows of the workload (same recipe; default: the workload's own B) -- for profiling "
+                         "a smaller case of the same kernels")
     a = ap.parse_args()
     a.warmup = max(3, a.warmup)
 
