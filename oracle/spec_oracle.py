@@ -49,6 +49,11 @@ the design notes):
       CDF edge of the chosen token (both on the normalised scale).
   R9  top-k keeps every token whose logit is >= the k-th largest logit (ties at
       the boundary are all kept); fewer than k finite logits keep everything.
+  R11 lenience l in (0, 1] multiplies q wherever it meets p: the accept test is
+      u <= min(1, p(x) / (l q(x))) and the residual is norm(max(0, p - l q)).
+      The pages state the scaling of q in the comparison and the resulting
+      guarantee (no token drawn with probability above p(x)/l), not the
+      residual; this residual is the plainest reading and meets the guarantee.
   R10 nucleus (top-p) keeps every token whose logit is >= that of the token at
       which the descending running probability first reaches top_p (ties kept);
       top_p >= 1 keeps everything.  A standardised row is the logit row with
@@ -166,7 +171,8 @@ def draw_candidates(w: np.ndarray, u: float) -> list[int]:
     return [int(k) for k in np.nonzero(ok)[0]]
 
 
-def verify_row(tl: np.ndarray, dl: np.ndarray, ids: np.ndarray, gb: int, u: np.ndarray, T: float):
+def verify_row(tl: np.ndarray, dl: np.ndarray, ids: np.ndarray, gb: int, u: np.ndarray, T: float,
+               lenience: float = 1.0):
     """Algorithm 1 Phases 3-4 for one row [p1 §2.3; p2 "The algorithm"; p3 §3].
 
     tl [gamma+1, V] and dl [gamma, V] float64 logits, ids [gamma], u [gamma+1]
@@ -201,7 +207,8 @@ def verify_row(tl: np.ndarray, dl: np.ndarray, ids: np.ndarray, gb: int, u: np.n
     for i in range(gb):
         x = int(ids[i])
         px, qx = p[i][x], q[i][x]
-        r = 1.0 if px >= qx else px / qx          # min(1, p/q) [p1 §2.3 Phase 3]
+        lq = lenience * qx                         # R11: lenience scales q [p1 §5, Appendix A.5]
+        r = 1.0 if px >= lq else px / lq          # min(1, p/q) [p1 §2.3 Phase 3]
         if abs(u[i] - r) < BOUNDARY_EPS:
             boundary = True
         if not (px > 0.0 and u[i] <= r):          # R3
@@ -210,7 +217,7 @@ def verify_row(tl: np.ndarray, dl: np.ndarray, ids: np.ndarray, gb: int, u: np.n
 
     # Phase 4: residual on rejection, bonus from p_{gamma_b+1} otherwise.
     if n < gb:
-        w = np.maximum(0.0, p[n] - q[n])          # norm(max(0, p - q)) [p1 Phase 4; p3 §3]
+        w = np.maximum(0.0, p[n] - lenience * q[n])  # norm(max(0, p - q)) [p1 Phase 4; p3 §3]; R11
         if np.sum(w) <= Z_FLOOR:                  # R4 [p4]
             w = p[n]
     else:
@@ -275,7 +282,8 @@ def _draft_len(draft_len, B, gamma):
     return np.asarray(draft_len, dtype=np.int64)
 
 
-def verify_sample(target, draft, dtype, ids, draft_len, uniforms, T, rows=None, tthr=None, dthr=None):
+def verify_sample(target, draft, dtype, ids, draft_len, uniforms, T, rows=None, tthr=None, dthr=None,
+                  lenience=1.0):
     """spec_verify_sample's contract, row by row.  target [B,gamma+1,V], draft [B,gamma,V].
 
     tthr [B,gamma+1] / dthr [B,gamma] (float32, optional) standardise each logit row first: logits
@@ -304,7 +312,7 @@ def verify_sample(target, draft, dtype, ids, draft_len, uniforms, T, rows=None, 
             tb = np.stack([apply_threshold(tb[i], float(np.float32(tthr[b][i]))) for i in range(G1)])
         if dthr is not None and gamma > 0:
             db = np.stack([apply_threshold(db[i], float(np.float32(dthr[b][i]))) for i in range(gamma)])
-        res = verify_row(tb, db, ids[b], gb, u[b], float(np.float32(T)))
+        res = verify_row(tb, db, ids[b], gb, u[b], float(np.float32(T)), float(np.float32(lenience)))
         emitted[b] = res["emitted"]
         n_acc[b] = res["n"]
         boundary[b] = res["boundary"]

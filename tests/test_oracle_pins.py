@@ -487,3 +487,39 @@ def test_thresholded_sampler_draws_from_the_truncated_softmax():
     keep = wts >= 2.5
     p = np.where(keep, wts, 0) / wts[keep].sum()
     assert np.all(np.abs(counts - N * p) <= 1.0 + 1e-9)
+
+
+# ----------------------------------------------------------------------------- lenience (R11)
+
+def _lenient_run(l):
+    def run(tl, dl, ids, u):
+        return O.verify_row(tl, dl, ids, dl.shape[0], u, 1.0, lenience=l)
+    return run
+
+
+@pytest.mark.parametrize("l", [0.1, 0.5, 0.9])
+@pytest.mark.parametrize("case", list(all_small_cases(seed=13))[::2], ids=lambda c: f"V{c[0]}g{c[1]}")
+def test_lenience_keeps_the_pages_bound(case, l):
+    """[p1] Appendix A.5 as restated in §5: with lenience l no token is drawn with probability above
+    p(x)/l; the first guess is accepted with probability sum_x min(q(x), p(x)/l) (q multiplied by l
+    before the comparison)."""
+    V, gamma, p, q = case
+    law = measure_law(_lenient_run(l), p, q)
+    assert abs(sum(law.values()) - 1.0) < 1e-12
+    first = first_token_marginal(law, V)
+    assert np.all(first <= p[0] / l + 1e-12), (first, p[0] / l)
+    if gamma >= 1:
+        accept = sum(v for k, v in law.items() if len(k) >= 2)
+        assert accept == pytest.approx(np.minimum(q[0], p[0] / l).sum(), abs=1e-12)
+        # R11's first-token law: accepted mass min(q, p/l), then the rejection mass spread over the
+        # residual max(0, p - l q) normalised
+        acc = np.minimum(q[0], p[0] / l)
+        resid = np.maximum(0.0, p[0] - l * q[0])
+        R = 1.0 - acc.sum()
+        expect = acc + (R * resid / resid.sum() if resid.sum() > 0 else 0.0)
+        assert np.max(np.abs(first - expect)) < 1e-12
+
+
+def test_lenience_one_is_the_exact_method():
+    for V, gamma, p, q in list(all_small_cases(seed=17))[:6]:
+        assert measure_law(_lenient_run(1.0), p, q) == measure_law(_run_row, p, q)
