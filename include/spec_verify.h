@@ -189,6 +189,20 @@ int spec_sample_rows(const void* logits, int dtype, const float* uniforms, float
                      int R, int V, int32_t* tokens,
                      void* workspace, size_t ws_bytes, void* stream);
 
+/* Lenient verification (paper-graph-ui teardown §5 on Appendix A.5 "lenience"):
+ * q is multiplied by the lenience l in (0, 1] before it is compared with p, so
+ * guess x_i is accepted iff p_i(x_i) > 0 and u_i <= min(1, p_i(x_i) / (l q_i(x_i))),
+ * and a rejection draws from norm(max(0, p_n - l q_n)).  The pages state the
+ * scaled comparison and its guarantee -- no token is drawn with probability
+ * above p(x)/l -- but not the residual; scaling q there too is the plainest
+ * reading and keeps the guarantee.  l = 1 is spec_verify_sample exactly.  Other
+ * arguments as spec_verify_sample; lenience outside (0, 1] returns SPEC_ERR_ARG. */
+int spec_verify_sample_lenient(const void* target_logits, const void* draft_logits, int dtype,
+                               const int32_t* draft_ids, const int32_t* draft_len, const float* uniforms,
+                               float temperature, float lenience, int B, int gamma, int V,
+                               int32_t* emitted, int32_t* n_accepted,
+                               void* workspace, size_t ws_bytes, void* stream);
+
 /* Top-k and nucleus (top-p) standardisation (paper-graph-ui teardown §2.2
  * "Standardized Sampling": keep the k largest probabilities, or the shortest
  * descending prefix whose mass reaches top_p, and renormalise).  Softmax is

@@ -61,6 +61,8 @@ def _load() -> ctypes.CDLL:
     L.spec_sample_rows_masked.restype = i32
     L.spec_verify_sample_masked.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, f32, i32, i32, i32, vp, vp, vp, sz, vp]
     L.spec_verify_sample_masked.restype = i32
+    L.spec_verify_sample_lenient.argtypes = [vp, vp, i32, vp, vp, vp, f32, f32, i32, i32, i32, vp, vp, vp, sz, vp]
+    L.spec_verify_sample_lenient.restype = i32
     L.spec_topk_threshold.argtypes = [vp, i32, i32, i32, i32, vp, vp]
     L.spec_topk_threshold.restype = i32
     L.spec_topp_threshold.argtypes = [vp, i32, f32, f32, i32, i32, vp, vp]
@@ -229,7 +231,8 @@ def _common(target, draft, ids, draft_len, gamma_needs_draft=True):
 def verify_sample(target: torch.Tensor, draft: torch.Tensor, ids: torch.Tensor, uniforms: torch.Tensor,
                   temperature: float, draft_len: torch.Tensor | None = None, *, emitted=None, n_accepted=None,
                   workspace: torch.Tensor | None = None, check: bool = False, phase: str = "both",
-                  target_thr: torch.Tensor | None = None, draft_thr: torch.Tensor | None = None):
+                  target_thr: torch.Tensor | None = None, draft_thr: torch.Tensor | None = None,
+                  lenience: float = 1.0):
     """spec_verify_sample: returns (emitted [B, gamma+1] int32, n_accepted [B] int32).
 
     phase="stream" / "draw" calls spec_verify_sample_stream / spec_verify_sample_draw: the two halves
@@ -247,6 +250,17 @@ def verify_sample(target: torch.Tensor, draft: torch.Tensor, ids: torch.Tensor, 
     _cuda(emitted, "emitted", torch.int32, (B, G + 1))
     _cuda(n_accepted, "n_accepted", torch.int32, (B,))
     ws = workspace if workspace is not None else workspace_for(dev, workspace_size(B, G, V, target.dtype))
+    if lenience != 1.0:  # spec_verify_sample_lenient
+        if phase != "both" or target_thr is not None or draft_thr is not None:
+            raise ValueError("lenience goes with phase='both' and no thresholds")
+        code = lib.spec_verify_sample_lenient(_p(target), _p(draft) if G > 0 else None, _dtype_code(target),
+                                              _p(ids) if G > 0 else None, _p(draft_len), _p(uniforms),
+                                              float(temperature), float(lenience), B, G, V, _p(emitted),
+                                              _p(n_accepted), _p(ws), ws.numel(), _stream(dev))
+        _raise(code, "spec_verify_sample_lenient")
+        if check:
+            check_status(ws)
+        return emitted, n_accepted
     if target_thr is not None or draft_thr is not None:  # spec_verify_sample_masked
         if phase != "both":
             raise ValueError("standardisation thresholds go with phase='both'")

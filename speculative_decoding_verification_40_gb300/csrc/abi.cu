@@ -239,10 +239,12 @@ int run_verify(const void* target, const void* draft, int dtype, const int32_t* 
                const float* uniforms, float temperature, int B, int gamma, int V, int32_t* emitted,
                int32_t* n_accepted, float* beta, float* p_draft, float* q_draft, float* accept_prob,
                float* resid, void* workspace, size_t ws_bytes, void* stream, bool stats, int phases = 3,
-               bool early_exit = false, const float* tthr = nullptr, const float* dthr = nullptr) {
+               bool early_exit = false, const float* tthr = nullptr, const float* dthr = nullptr,
+               float lenience = 1.f) {
   int st = check_common(dtype, B, gamma, V, workspace, ws_bytes);
   if (st != SPEC_OK) return st;
   if (!(std::isfinite(temperature) && temperature > 0.f)) return SPEC_ERR_ARG;
+  if (!(lenience > 0.f && lenience <= 1.f)) return SPEC_ERR_ARG;
   if (B == 0 || (stats && gamma == 0)) return SPEC_OK;
   if (target == nullptr) return SPEC_ERR_ARG;
   if (gamma > 0 && (draft == nullptr || ids == nullptr)) return SPEC_ERR_ARG;
@@ -260,6 +262,7 @@ int run_verify(const void* target, const void* draft, int dtype, const int32_t* 
     p.tthr = tthr;
     p.dthr = gamma > 0 ? dthr : nullptr;
     p.scale = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+    p.lq = lenience;
     p.B = B;
     p.G = gamma;
     p.V = V;
@@ -369,6 +372,15 @@ int spec_verify_sample_masked(const void* target_logits, const void* draft_logit
   return run_verify(target_logits, draft_logits, dtype, draft_ids, draft_len, uniforms, temperature, B, gamma, V,
                     emitted, n_accepted, nullptr, nullptr, nullptr, nullptr, nullptr, workspace, ws_bytes, stream,
                     false, 3, false, target_thr, draft_thr);
+}
+
+int spec_verify_sample_lenient(const void* target_logits, const void* draft_logits, int dtype,
+                               const int32_t* draft_ids, const int32_t* draft_len, const float* uniforms,
+                               float temperature, float lenience, int B, int gamma, int V, int32_t* emitted,
+                               int32_t* n_accepted, void* workspace, size_t ws_bytes, void* stream) {
+  return run_verify(target_logits, draft_logits, dtype, draft_ids, draft_len, uniforms, temperature, B, gamma, V,
+                    emitted, n_accepted, nullptr, nullptr, nullptr, nullptr, nullptr, workspace, ws_bytes, stream,
+                    false, 3, false, nullptr, nullptr, lenience);
 }
 
 int spec_topk_threshold(const void* logits, int dtype, int R, int V, int k, float* thr, void* stream) {

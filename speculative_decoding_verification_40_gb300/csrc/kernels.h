@@ -47,6 +47,7 @@ struct SampleParams {
   const float* tthr;         // [B, G+1] standardisation thresholds of the target rows, or nullptr
   const float* dthr;         // [B, G] standardisation thresholds of the draft rows, or nullptr
   float scale;               // log2(e) / T
+  float lq;                  // lenience l in (0, 1]: q enters the accept test and the residual as l q
   int B, G, V;
   int slice;                 // vocabulary elements per work item (a multiple of 32 x elements per 16 bytes)
   int nslices;               // stream CTAs per logit row (<= kMaxSlices)

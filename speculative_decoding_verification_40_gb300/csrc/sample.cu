@@ -126,7 +126,7 @@ __device__ __forceinline__ int accept_position(const SampleParams& a, int b, int
   const float sc = a.scale;
   const float2 xl = __ldcg(reinterpret_cast<const float2*>(a.ws.xl) + (size_t)b * a.G + i);
   const float px = fast_exp2((xl.x - nm.x) * sc) / nm.y;
-  const float qx = fast_exp2((xl.y - nm.z) * sc) / nm.w;
+  const float qx = fast_exp2((xl.y - nm.z) * sc) / nm.w * a.lq;  // l q(x) (l = 1 unless lenient)
   const float ratio = px >= qx ? 1.f : px / qx;  // min(1, p/q); q = 0 < p gives 1
   return (px > 0.f && ui <= ratio) ? 1 : 0;
 }
@@ -188,7 +188,7 @@ __device__ RowState decide_row(const SampleParams& a, int b, int gb, DrawSmem& s
     st.dt = -INFINITY;
     if (n < gb) {
       st.mq = sm.mq[n];
-      st.iq = 1.f / sm.sq[n];
+      st.iq = a.lq / sm.sq[n];  // the residual's q is l q
       if (a.dthr) st.dt = __ldg(a.dthr + (size_t)b * a.G + n);
     }
   }

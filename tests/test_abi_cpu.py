@@ -131,3 +131,10 @@ def test_sample_rows_rejects_bad_arguments_on_the_host():
     assert call(ws=None) == 7
     assert call(wsb=16) == 7
     assert call(R=0, logits=None, u=None, tok=None, ws=None, wsb=0) == 0
+
+
+def test_lenient_rejects_lenience_outside_unit_interval():
+    L = S.lib
+    p = ctypes.c_void_p(4096)
+    for l in (0.0, -0.5, 1.5, float("nan")):
+        assert L.spec_verify_sample_lenient(p, p, 0, p, None, p, 1.0, l, 2, 3, 100, p, p, FAKE_WS, BIG, None) == 1
