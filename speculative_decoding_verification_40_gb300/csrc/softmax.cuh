@@ -7,6 +7,29 @@
 
 namespace specv {
 
+// Packed pairs of float32 (sm_100 family f32x2 arithmetic): lane 0 in the low word.
+__device__ __forceinline__ unsigned long long pack2(float lo, float hi) {
+  unsigned long long v;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(lo), "f"(hi));
+  return v;
+}
+
+__device__ __forceinline__ void unpack2(unsigned long long v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b, unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -96,15 +119,36 @@ __device__ __forceinline__ void online_group(float& m, float& s, float& raw, con
       m = vm;
     }
     const float nc = -m * sc;
-    float a0 = 0.f, a1 = 0.f;
+    float a0 = 0.f, a1 = 0.f;  // even elements accumulate in a0, odd in a1
+    if constexpr (sizeof(T) == 2) {
+      // bfloat16 carries twice the elements per byte: pairs go through the packed f32x2 FMA / add (two
+      // float32 lanes, the same rounding as two scalar operations), fewer instructions per element
+      const unsigned long long sc2 = pack2(sc, sc), nc2 = pack2(nc, nc);
+      unsigned long long acc = 0ull;
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      float f[kV];
-      Elems<T>::widen(r[u], f);
+      for (int u = 0; u < U; ++u) {
+        float f[kV];
+        Elems<T>::widen(r[u], f);
 #pragma unroll
-      for (int j = 0; j < kV; j += 2) {
-        a0 += fast_exp2(fmaf(kMask ? masked(f[j], thr) : f[j], sc, nc));
-        a1 += fast_exp2(fmaf(kMask ? masked(f[j + 1], thr) : f[j + 1], sc, nc));
+        for (int j = 0; j < kV; j += 2) {
+          const unsigned long long x =
+              pack2(kMask ? masked(f[j], thr) : f[j], kMask ? masked(f[j + 1], thr) : f[j + 1]);
+          float t0, t1;
+          unpack2(fma2(x, sc2, nc2), t0, t1);
+          acc = add2(acc, pack2(fast_exp2(t0), fast_exp2(t1)));
+        }
+      }
+      unpack2(acc, a0, a1);
+    } else {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        float f[kV];
+        Elems<T>::widen(r[u], f);
+#pragma unroll
+        for (int j = 0; j < kV; j += 2) {
+          a0 += fast_exp2(fmaf(kMask ? masked(f[j], thr) : f[j], sc, nc));
+          a1 += fast_exp2(fmaf(kMask ? masked(f[j + 1], thr) : f[j + 1], sc, nc));
+        }
       }
     }
     s += a0 + a1;

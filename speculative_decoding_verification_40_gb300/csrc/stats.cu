@@ -45,12 +45,27 @@ constexpr int kMinBlocks = 4;  // resident CTAs per SM the register budget is si
 template <int kV>
 __device__ __forceinline__ void overlap(const float* f, const float* g, float sc, float ncp, float ncq, float& tmin,
                                         float& tp) {
+  if constexpr (kV == 8) {
+    // bfloat16 rows: (p, q) and (min, p) pairs through the packed f32x2 FMA / add, the same rounding as
+    // the scalar operations
+    const unsigned long long sc2 = pack2(sc, sc), nc2 = pack2(ncp, ncq);
+    unsigned long long acc = pack2(tmin, tp);
 #pragma unroll
-  for (int j = 0; j < kV; ++j) {
-    const float p = fast_exp2(fmaf(f[j], sc, ncp));
-    const float q = fast_exp2(fmaf(g[j], sc, ncq));
-    tmin += fminf(p, q);
-    tp += p;
+    for (int j = 0; j < kV; ++j) {
+      float ep, eq;
+      unpack2(fma2(pack2(f[j], g[j]), sc2, nc2), ep, eq);
+      const float p = fast_exp2(ep), q = fast_exp2(eq);
+      acc = add2(acc, pack2(fminf(p, q), p));
+    }
+    unpack2(acc, tmin, tp);
+  } else {
+#pragma unroll
+    for (int j = 0; j < kV; ++j) {
+      const float p = fast_exp2(fmaf(f[j], sc, ncp));
+      const float q = fast_exp2(fmaf(g[j], sc, ncq));
+      tmin += fminf(p, q);
+      tp += p;
+    }
   }
 }
 
