@@ -46,7 +46,7 @@ enum : int { kRowInvalid = 1, kRowResid = 2 };
 struct RowState {
   int n, flags;
   uint32_t err;
-  float mp, ip, mq, iq;
+  float nmp, ip, nmq, iq;  // p = 2^(l log2(e)/T + nmp) * ip (nmp = -m_p log2(e)/T, ip = 1/S_p); q likewise
   float tt, dt;  // standardisation thresholds of the drawn target / draft row (-inf: none)
 };
 
@@ -71,8 +71,10 @@ __device__ __forceinline__ void seg_weights(const T* tr, const T* dr, bool resid
   }
 #pragma unroll
   for (int j = 0; j < kV; ++j) {
-    p[j] = fast_exp2((masked(lt[j], st.tt) - st.mp) * sc) * st.ip;
-    w[j] = resid ? fmaxf(p[j] - fast_exp2((masked(ld[j], st.dt) - st.mq) * sc) * st.iq, 0.f) : p[j];
+    // separately rounded products (no contraction into the subtraction): the chunk-mass pass, scalar or
+    // packed, computes exactly these values
+    p[j] = __fmul_rn(fast_exp2(fmaf(masked(lt[j], st.tt), sc, st.nmp)), st.ip);
+    w[j] = resid ? fmaxf(p[j] - __fmul_rn(fast_exp2(fmaf(masked(ld[j], st.dt), sc, st.nmq)), st.iq), 0.f) : p[j];
   }
 }
 
@@ -182,12 +184,12 @@ __device__ RowState decide_row(const SampleParams& a, int b, int gb, DrawSmem& s
     st.flags = kRowInvalid;
   } else {
     st.flags = n < gb ? kRowResid : 0;
-    st.mp = sm.mp[n];
+    st.nmp = -sm.mp[n] * a.scale;
     st.ip = 1.f / sm.sp[n];
     st.tt = a.tthr ? __ldg(a.tthr + (size_t)b * G1 + n) : -INFINITY;
     st.dt = -INFINITY;
     if (n < gb) {
-      st.mq = sm.mq[n];
+      st.nmq = -sm.mq[n] * a.scale;
       st.iq = a.lq / sm.sq[n];  // the residual's q is l q
       if (a.dthr) st.dt = __ldg(a.dthr + (size_t)b * a.G + n);
     }
@@ -579,12 +581,29 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_draw_kernel(const Sa
           Elems<T>::widen(rt[r], lt);
           if (resid) Elems<T>::widen(rd[r], ld);
           float sw = 0.f, spp = 0.f;
+          if constexpr (sizeof(T) == 2) {
+            // bfloat16: (p, q) pairs through the packed f32x2 FMA / multiply -- per lane the same
+            // operations as seg_weights, so the chunk masses and the final scan see identical weights
+            const unsigned long long sc2 = pack2(sc, sc), nm2 = pack2(st.nmp, st.nmq), i2 = pack2(st.ip, st.iq);
 #pragma unroll
-          for (int j = 0; j < kV; ++j) {
-            const float p = fast_exp2((masked(lt[j], st.tt) - st.mp) * sc) * st.ip;
-            const float w = resid ? fmaxf(p - fast_exp2((masked(ld[j], st.dt) - st.mq) * sc) * st.iq, 0.f) : p;
-            sw += w;
-            spp += p;
+            for (int j = 0; j < kV; ++j) {
+              float ep, eq, p, q;
+              unpack2(fma2(pack2(masked(lt[j], st.tt), resid ? masked(ld[j], st.dt) : -INFINITY), sc2, nm2), ep,
+                      eq);
+              unpack2(mul2(pack2(fast_exp2(ep), fast_exp2(eq)), i2), p, q);
+              const float w = resid ? fmaxf(p - q, 0.f) : p;
+              sw += w;
+              spp += p;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < kV; ++j) {
+              const float p = __fmul_rn(fast_exp2(fmaf(masked(lt[j], st.tt), sc, st.nmp)), st.ip);
+              const float w =
+                  resid ? fmaxf(p - __fmul_rn(fast_exp2(fmaf(masked(ld[j], st.dt), sc, st.nmq)), st.iq), 0.f) : p;
+              sw += w;
+              spp += p;
+            }
           }
           lw += sw;
           lp += spp;
