@@ -306,17 +306,33 @@ def run_ours(a, rank, world, dist):
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_em.numel() * 4 + out_na.numel() * 4
 
+    # Rows are independent, so the batch goes over in four row groups: group g is verified (one
+    # spec_verify_sample call on its rows) while group g+1 is still being copied.  The host link, not
+    # the GPU, bounds this number: pinned host memory reaches about 210 GB/s on this system.
+    groups = [(g * w.B // 4, (g + 1) * w.B // 4) for g in range(4) if (g + 1) * w.B // 4 > g * w.B // 4]
+    copy_stream = torch.cuda.Stream(dev)
+    ws_g = S.workspace_for(dev, S.workspace_size(w.B, w.gamma, w.V, w.target.dtype))
+    copied = [torch.cuda.Event() for _ in groups]
+
     def e2e_step():
-        for n, t in host.items():
-            dev_in[n].copy_(t, non_blocking=True)
-        S.verify_sample(dev_in["target"], dev_in["draft"], dev_in["ids"], dev_in["uniforms"], w.T,
-                        dev_in.get("draft_len"), emitted=em, n_accepted=na, workspace=ws)
+        copy_stream.wait_stream(stream)
+        with torch.cuda.stream(copy_stream):
+            for gi, (lo, hi) in enumerate(groups):
+                for n, t in host.items():
+                    dev_in[n][lo:hi].copy_(t[lo:hi], non_blocking=True)
+                copied[gi].record(copy_stream)
+        for gi, (lo, hi) in enumerate(groups):
+            stream.wait_event(copied[gi])
+            S.verify_sample(dev_in["target"][lo:hi], dev_in["draft"][lo:hi], dev_in["ids"][lo:hi],
+                            dev_in["uniforms"][lo:hi], w.T,
+                            None if "draft_len" not in dev_in else dev_in["draft_len"][lo:hi],
+                            emitted=em[lo:hi], n_accepted=na[lo:hi], workspace=ws_g)
         out_em.copy_(em, non_blocking=True)
         out_na.copy_(na, non_blocking=True)
 
     e2e_steps = max(3, min(a.steps, 20))
     e2e_ms = time_device(e2e_step, e2e_steps, 2, stream)
-    assert S.check_status(ws) == 0
+    assert S.check_status(ws_g) == 0
     _, e2e_units = combine_ranks(e2e_ms, float(pos), dist, dev)
 
     # the variants, one call each per step on the same batch (context for the line)
