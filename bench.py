@@ -203,12 +203,15 @@ def oracle_pool(procs: int):
 def _oracle_rows(args):
     import oracle as O
     target, draft, dtype, ids, gl, u, T = args
-    O.verify_sample(target, draft, dtype, ids, gl, u, T)
-    return target.shape[0]
+    r = O.verify_sample(target, draft, dtype, ids, gl, u, T)
+    return r["emitted"], r["n_accepted"], r["boundary"]
 
 
-def cpu_oracle_rate(w: W.Workload, rows: int, procs: int, pool=None) -> dict:
-    """Oracle positions/s over the first `rows` rows (repeated over the batch as needed), on `procs` processes."""
+def cpu_oracle_rate(w: W.Workload, rows: int, procs: int, pool=None, gpu=None) -> dict:
+    """Oracle positions/s over the first `rows` rows (repeated over the batch as needed), on `procs` processes.
+
+    With gpu = (emitted, n_accepted) of the same batch, the oracle's outputs on the distinct rows of the
+    sample are compared with the GPU's (token-exact outside the oracle's boundary rows) and counted."""
     h = {"target": W.logits_as_numpy(w.target), "draft": W.logits_as_numpy(w.draft),
          "ids": w.ids.cpu().numpy(), "gl": None if w.draft_len is None else w.draft_len.cpu().numpy(),
          "u": w.uniforms.cpu().numpy()}
@@ -220,21 +223,35 @@ def cpu_oracle_rate(w: W.Workload, rows: int, procs: int, pool=None) -> dict:
     positions = sum(w.gamma if h["gl"] is None else int(h["gl"][r]) for r in idx)
     if procs <= 1:
         t0 = time.perf_counter()
-        for j in jobs:
-            _oracle_rows(j)
+        res = [_oracle_rows(j) for j in jobs]
         dt = time.perf_counter() - t0
     elif pool is not None:
         t0 = time.perf_counter()
-        pool.map(_oracle_rows, jobs)
+        res = pool.map(_oracle_rows, jobs)
         dt = time.perf_counter() - t0
     else:
         with oracle_pool(procs) as pool:
             pool.map(_oracle_rows, jobs[:procs])       # start-up and imports outside the timing
             t0 = time.perf_counter()
-            pool.map(_oracle_rows, jobs)
+            res = pool.map(_oracle_rows, jobs)
             dt = time.perf_counter() - t0
-    return {"value": positions / dt, "unit": UNIT, "cores": procs, "kind": "oracle",
-            "sample": f"{rows} rows of {w.name} (float64 numpy oracle, {positions} positions) in {dt:.2f} s"}
+    out = {"value": positions / dt, "unit": UNIT, "cores": procs, "kind": "oracle",
+           "sample": f"{rows} rows of {w.name} (float64 numpy oracle, {positions} positions) in {dt:.2f} s"}
+    if gpu is not None:
+        em, na = (t.cpu().numpy() for t in gpu)
+        seen, checked, boundary, mism = set(), 0, 0, 0
+        for c, (r_em, r_na, r_bd) in zip(chunks, res):
+            for j, b in enumerate(c):
+                if b in seen:
+                    continue
+                seen.add(b)
+                checked += 1
+                if r_bd[j]:
+                    boundary += 1
+                elif int(na[b]) != int(r_na[j]) or list(em[b]) != list(r_em[j]):
+                    mism += 1
+        out["parity"] = {"rows_compared": checked, "boundary_rows": boundary, "mismatches": mism}
+    return out
 
 
 # ----------------------------------------------------------------------------- arms
@@ -417,7 +434,11 @@ def run_ours(a, rank, world, dist):
         "also": also,
     }
     if rank == 0 and not a.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_oracle_rate(w, a.cpu_rows, os.cpu_count() or 1)
+        # the batch's plain outputs again (the variants above reused the output buffers)
+        S.verify_sample(w.target, w.draft, w.ids, w.uniforms, w.T, w.draft_len, emitted=em, n_accepted=na,
+                        workspace=ws)
+        assert S.check_status(ws) == 0
+        line["cpu_baseline"] = cpu_oracle_rate(w, a.cpu_rows, os.cpu_count() or 1, gpu=(em, na))
     return line
 
 
