@@ -27,11 +27,15 @@ __all__ = [
     "optimal_gamma", "alpha_mean", "topk_threshold", "topp_threshold",
 ]
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libspecverify.so")
+# SPECVERIFY_DEBUG_BOUNDS=1 loads the debug-bounds build (kernel index checks that report SPEC_ERR_BOUNDS
+# instead of accessing out of range; `build.py --debug-bounds`)
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                        "libspecverify_debug.so" if os.environ.get("SPECVERIFY_DEBUG_BOUNDS") == "1"
+                        else "libspecverify.so")
 
 SPEC_F32, SPEC_BF16 = 0, 1
 STATUS = {0: "ok", 1: "invalid argument", 2: "unknown dtype", 3: "CUDA error", 4: "non-finite or all -inf logit row",
-          5: "draft id outside [0, V)", 6: "timeout", 7: "workspace too small or misaligned"}
+          5: "draft id outside [0, V)", 6: "timeout", 7: "workspace too small or misaligned", 8: "index check failed"}
 
 
 class SpecVerifyError(RuntimeError):
@@ -43,7 +47,8 @@ class SpecVerifyError(RuntimeError):
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is missing: build it with "
-                          "`python speculative_decoding_verification_40_gb300/build.py`")
+                          "`python speculative_decoding_verification_40_gb300/build.py`"
+                          + (" --debug-bounds" if LIB_PATH.endswith("_debug.so") else ""))
     L = ctypes.CDLL(LIB_PATH)
     vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     L.spec_workspace_size.argtypes = [i32, i32, i32, i32]

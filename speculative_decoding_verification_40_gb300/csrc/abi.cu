@@ -519,6 +519,7 @@ const char* spec_status_string(int status) {
     case SPEC_ERR_TOKEN_RANGE: return "draft id outside [0, V)";
     case SPEC_ERR_TIMEOUT: return "timeout";
     case SPEC_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case SPEC_ERR_BOUNDS: return "index check failed";
     default: return "unknown status";
   }
 }

@@ -22,6 +22,13 @@ constexpr uint32_t kErrArg = 1u << 1;
 constexpr uint32_t kErrNonfinite = 1u << 4;
 constexpr uint32_t kErrToken = 1u << 5;
 constexpr uint32_t kErrTimeout = 1u << 6;
+constexpr uint32_t kErrBounds = 1u << 8;   // debug-bounds builds: an index check failed (access skipped)
+
+#ifdef SPEC_DEBUG_BOUNDS
+constexpr bool kDebugBounds = true;
+#else
+constexpr bool kDebugBounds = false;
+#endif
 
 // Residual-mass floor below which the draw falls back to p (interactiveml correction rule).
 constexpr float kZFloor = 1e-15f;
@@ -163,6 +170,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
     if (done) return true;
   }
   return false;
+}
+
+// Index check of debug-bounds builds (-DSPEC_DEBUG_BOUNDS): a false condition records kErrBounds in the
+// error word and returns false, and the caller skips the access.  In normal builds it is always true and
+// compiles away.  Conditions are uniform over a CTA where the caller returns before a barrier.
+__device__ __forceinline__ bool bounds_ok(bool cond, uint32_t* err) {
+  if (kDebugBounds && !cond) {
+    atomicOr(err, kErrBounds);
+    return false;
+  }
+  return true;
 }
 
 // max that propagates NaN: a NaN anywhere in a row survives the reduction.

@@ -118,6 +118,7 @@ __global__ void __launch_bounds__(kGreedyThreads) greedy_rows_kernel(const Greed
 
   const int lo = s * a.slice;
   const int n = min(a.V, lo + a.slice) - lo;
+  if (!bounds_ok(b < a.B && n > 0 && lo + n <= a.V, a.ws.err)) return;
   const T* src = reinterpret_cast<const T*>(a.target) + ((size_t)b * G1 + i) * a.V + lo;
   constexpr int kV = Elems<T>::kVec;
   constexpr int U = 4;

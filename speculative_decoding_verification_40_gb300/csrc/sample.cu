@@ -331,6 +331,7 @@ __device__ void resolve_row(const SampleParams& a, int b, int gb, const RowState
       }
     }
     if (tok < 0) tok = lasttok;
+    if (!bounds_ok(tok < a.V, a.ws.err)) tok = -1;
     if (lane == 0) {
       if (tok >= 0) {
         for (int j = 0; j < st.n; ++j) e[j] = __ldg(a.ids + (size_t)b * a.G + j);
@@ -487,6 +488,7 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_stream_kernel(const 
   const float sc = a.scale;
   const int lo = s * a.slice;
   const int n = min(a.V, lo + a.slice) - lo;
+  if (!bounds_ok(b < a.B && i <= a.G && s < NS && NS <= kMaxSlices && n > 0 && lo + n <= a.V, a.ws.err)) return;
   const T* tp = reinterpret_cast<const T*>(a.target) + ((size_t)b * G1 + i) * a.V + lo;
   const T* dp = has_q ? reinterpret_cast<const T*>(a.draft) + ((size_t)b * a.G + i) * a.V + lo : tp;
 
@@ -565,6 +567,8 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_draw_kernel(const Sa
     const int cps = a.dslice / cpc;              // chunks per slice
     const int c0 = d * cps;
     const int c1 = min(c0 + cps, (a.V + cpc - 1) / cpc);
+    if (!bounds_ok(cps <= kMaxChunksPerSlice && (size_t)ND * cps <= chunks_per_row(a.V) && st.n <= gb, a.ws.err))
+      return;
     const float sc = a.scale;
     for (int c = c0 + warp; c < c1; c += kSW) {
       float lw = 0.f, lp = 0.f;
@@ -909,7 +913,7 @@ __global__ void __launch_bounds__(kST) sample_rows_fused_kernel(const SamplePara
   const int lo = sh_w * segE;
   const int n = min(V, lo + segE) - lo;
   const int tok = draw_in_slice<T>(row + lo, n, vec, sc, -sh_m * sc, thr, sh_t, cm);
-  if (tid == 0) a.emitted[b] = tok >= 0 ? lo + tok : -1;
+  if (tid == 0) a.emitted[b] = (tok >= 0 && bounds_ok(lo + tok < V, a.ws.err)) ? lo + tok : -1;
 }
 
 // Rows longer than one slice, pass 1: one CTA per (row b, slice s); warp w writes the normaliser of
@@ -925,6 +929,7 @@ __global__ void __launch_bounds__(kST, 4) sample_stream_kernel(const SampleParam
   const int segE = segment_len<T>(a.slice);
   const int lo = s * a.slice + warp * segE;
   const int hi = min(a.V, min(s * a.slice + a.slice, lo + segE));
+  if (!bounds_ok(b < a.B && (size_t)NS * kSW <= chunks_per_row(a.V), a.ws.err)) return;
   float m, sm, raw;
   const float thr = kMask && a.tthr ? __ldg(a.tthr + b) : -INFINITY;
   warp_segment<T, kMask>(reinterpret_cast<const T*>(a.target) + (size_t)b * a.V + lo, hi - lo, a.vec != 0, a.scale,
@@ -995,10 +1000,14 @@ __global__ void __launch_bounds__(kST) sample_rows_kernel(const SampleParams a) 
   const int segE = segment_len<T>(a.slice);
   const int lo = s * a.slice + w * segE;
   const int n = min(a.V, min(s * a.slice + a.slice, lo + segE)) - lo;
+  if (!bounds_ok(g >= 0 && g < NG && n > 0 && segE <= kMaxChunksPerSlice * kR * 32 * Elems<T>::kVec, a.ws.err)) {
+    if (tid == 0) a.emitted[b] = -1;
+    return;
+  }
   const T* srow = reinterpret_cast<const T*>(a.target) + (size_t)b * a.V + lo;
   const float thr = a.tthr ? __ldg(a.tthr + b) : -INFINITY;
   const int tok = draw_in_slice<T>(srow, n, a.vec != 0, sc, -M * sc, thr, beyond ? INFINITY : sh_t, cm);
-  if (tid == 0) a.emitted[b] = tok >= 0 ? lo + tok : -1;
+  if (tid == 0) a.emitted[b] = (tok >= 0 && bounds_ok(lo + tok < a.V, a.ws.err)) ? lo + tok : -1;
 }
 
 template <typename T>

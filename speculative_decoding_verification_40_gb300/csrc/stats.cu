@@ -111,6 +111,8 @@ __global__ void __launch_bounds__(kT, kMinBlocks) stats_rows_kernel(const Verify
   }
   const int lo = rank * a.L;
   const int n = max(0, min(a.V, lo + a.L) - lo);
+  // uniform over the cluster (the same sizes in every CTA), so the whole cluster leaves together
+  if (!bounds_ok(pos < a.B * a.G && CS <= kMaxCluster && (long long)CS * a.L >= a.V, a.ws.err)) return;
   const float sc = a.scale;
   const T* tp = reinterpret_cast<const T*>(a.target) + ((size_t)b * G1 + i) * a.V + lo;
   const T* dp = reinterpret_cast<const T*>(a.draft) + (size_t)pos * a.V + lo;

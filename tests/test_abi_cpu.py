@@ -97,7 +97,7 @@ def test_greedy_and_stats_reject_bad_arguments():
 
 
 def test_status_strings():
-    for code in range(8):
+    for code in range(9):
         assert S.lib.spec_status_string(code).decode() == S.STATUS[code]
 
 
