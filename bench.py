@@ -256,6 +256,32 @@ def cpu_oracle_rate(w: W.Workload, rows: int, procs: int, pool=None, gpu=None) -
 
 # ----------------------------------------------------------------------------- arms
 
+def c0_latency(S, dev, stream, ncalls: int = 50, reps: int = 20) -> dict:
+    """c0 (B=1, gamma=4, V=1024): microseconds per call over independent calls, launched one by one and
+    replayed from a captured CUDA graph (the library's calls are launches only, so they capture)."""
+    calls = [W.make(0, device=dev, call=c) for c in range(ncalls)]
+    ws = S.workspace_for(dev, S.workspace_size(1, 4, 1024, torch.float32))
+    em = torch.empty(1, 5, dtype=torch.int32, device=dev)
+    na = torch.empty(1, dtype=torch.int32, device=dev)
+
+    def run_all():
+        for w in calls:
+            S.verify_sample(w.target, w.draft, w.ids, w.uniforms, w.T, emitted=em, n_accepted=na, workspace=ws)
+
+    plain = time_device(run_all, reps, 3, stream) * 1e3 / ncalls
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        run_all()                                   # first calls (plan caches) outside the capture
+    stream.wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run_all()
+    graphed = time_device(graph.replay, reps, 3, stream) * 1e3 / ncalls
+    assert S.check_status(ws) == 0
+    return {"us_per_call": round(plain, 2), "us_per_call_cuda_graph": round(graphed, 2), "calls": ncalls}
+
+
 def run_ours(a, rank, world, dist):
     import speculative_decoding_verification_40_gb300 as S
     dev = torch.device("cuda", torch.cuda.current_device())
@@ -399,6 +425,8 @@ def run_ours(a, rank, world, dist):
             del w2
         assert S.check_status(ws2) == 0
 
+    if not a.no_also:
+        also["c0"] = c0_latency(S, dev, stream)
     line = {
         "metric": METRIC, "value": units / t_max, "unit": UNIT, "n_gpus": world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
