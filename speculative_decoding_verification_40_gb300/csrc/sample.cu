@@ -46,7 +46,7 @@ enum : int { kRowInvalid = 1, kRowResid = 2 };
 struct RowState {
   int n, flags;
   uint32_t err;
-  float nmp, ip, nmq, iq;  // p = 2^(l log2(e)/T + nmp) * ip (nmp = -m_p log2(e)/T, ip = 1/S_p); q likewise
+  float cp, cq;  // p = 2^(l log2(e)/T + cp), cp = -m_p log2(e)/T - log2 S_p; q likewise (times the lenience)
   float tt, dt;  // standardisation thresholds of the drawn target / draft row (-inf: none)
 };
 
@@ -71,10 +71,9 @@ __device__ __forceinline__ void seg_weights(const T* tr, const T* dr, bool resid
   }
 #pragma unroll
   for (int j = 0; j < kV; ++j) {
-    // separately rounded products (no contraction into the subtraction): the chunk-mass pass, scalar or
-    // packed, computes exactly these values
-    p[j] = __fmul_rn(fast_exp2(fmaf(masked(lt[j], st.tt), sc, st.nmp)), st.ip);
-    w[j] = resid ? fmaxf(p[j] - __fmul_rn(fast_exp2(fmaf(masked(ld[j], st.dt), sc, st.nmq)), st.iq), 0.f) : p[j];
+    // one FFMA and one exp2 per probability; the chunk-mass pass, scalar or packed, computes exactly these
+    p[j] = fast_exp2(fmaf(masked(lt[j], st.tt), sc, st.cp));
+    w[j] = resid ? fmaxf(p[j] - fast_exp2(fmaf(masked(ld[j], st.dt), sc, st.cq)), 0.f) : p[j];
   }
 }
 
@@ -184,13 +183,11 @@ __device__ RowState decide_row(const SampleParams& a, int b, int gb, DrawSmem& s
     st.flags = kRowInvalid;
   } else {
     st.flags = n < gb ? kRowResid : 0;
-    st.nmp = -sm.mp[n] * a.scale;
-    st.ip = 1.f / sm.sp[n];
+    st.cp = -sm.mp[n] * a.scale - log2f(sm.sp[n]);
     st.tt = a.tthr ? __ldg(a.tthr + (size_t)b * G1 + n) : -INFINITY;
     st.dt = -INFINITY;
     if (n < gb) {
-      st.nmq = -sm.mq[n] * a.scale;
-      st.iq = a.lq / sm.sq[n];  // the residual's q is l q
+      st.cq = -sm.mq[n] * a.scale - log2f(sm.sq[n]) + log2f(a.lq);  // the residual's q is l q
       if (a.dthr) st.dt = __ldg(a.dthr + (size_t)b * a.G + n);
     }
   }
@@ -215,6 +212,37 @@ __device__ void resolve_row(const SampleParams& a, int b, int gb, const RowState
   const bool failed = st.flags & kRowInvalid;
   if (!failed && tid < ND) sm.ds[tid] = __ldcg(dsum + tid);
   __syncthreads();
+  if (!failed && resid) {
+    // a residual whose mass is degenerate (<= 1e-15) draws from p instead; the draw CTAs summed only the
+    // residual, so this CTA sums the p masses of the row's chunks now (rare: a rejection implies a
+    // positive residual in exact arithmetic)
+    float Z = 0.f;
+    for (int d = 0; d < ND; ++d) Z += sm.ds[d].x;
+    if (!(Z > kZFloor)) {
+      const int warp = tid >> 5;
+      const T* tr = reinterpret_cast<const T*>(a.target) + ((size_t)b * G1 + st.n) * a.V;
+      for (int c = warp; c < ND * cps; c += kSW) {
+        float lp = 0.f;
+        if (c < nc) {
+#pragma unroll
+          for (int r = 0; r < kR; ++r) {
+            float pv[kV], wv[kV];
+            seg_weights<T>(tr, tr, false, a.V, a.vec != 0, c * cpc + r * seg + lane * kV, st, a.scale, pv, wv);
+            lp += lane_sum<kV>(pv);
+          }
+        }
+        lp = warp_sum(lp);
+        if (lane == 0) dch[c].y = lp;
+      }
+      __syncthreads();
+      if (tid < ND) {
+        float P = 0.f;
+        for (int c = 0; c < cps; ++c) P += __ldcg(&dch[tid * cps + c].y);
+        sm.ds[tid].y = P;
+      }
+      __syncthreads();
+    }
+  }
   if (!failed && tid == 0) {
     // total mass in slice order; the residual, or p when the residual mass is degenerate
     const float uf = __ldg(a.uniforms + (size_t)b * G1 + a.G);
@@ -584,33 +612,39 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_draw_kernel(const Sa
           float lt[kV], ld[kV];
           Elems<T>::widen(rt[r], lt);
           if (resid) Elems<T>::widen(rd[r], ld);
-          float sw = 0.f, spp = 0.f;
-          if constexpr (sizeof(T) == 2) {
-            // bfloat16: (p, q) pairs through the packed f32x2 FMA / multiply -- per lane the same
-            // operations as seg_weights, so the chunk masses and the final scan see identical weights
-            const unsigned long long sc2 = pack2(sc, sc), nm2 = pack2(st.nmp, st.nmq), i2 = pack2(st.ip, st.iq);
+          float sw = 0.f;
+          if (!resid) {
+            // bonus or p draw: the weights are p (pairs through the packed f32x2 FMA for bfloat16)
+            if constexpr (sizeof(T) == 2) {
+              const unsigned long long sc2 = pack2(sc, sc), c2 = pack2(st.cp, st.cp);
+#pragma unroll
+              for (int j = 0; j < kV; j += 2) {
+                float e0, e1;
+                unpack2(fma2(pack2(masked(lt[j], st.tt), masked(lt[j + 1], st.tt)), sc2, c2), e0, e1);
+                sw += fast_exp2(e0) + fast_exp2(e1);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < kV; ++j) sw += fast_exp2(fmaf(masked(lt[j], st.tt), sc, st.cp));
+            }
+          } else if constexpr (sizeof(T) == 2) {
+            // residual: (p, q) pairs through the packed FMA -- per lane the same operations as
+            // seg_weights, so the chunk masses and the final scan see identical weights
+            const unsigned long long sc2 = pack2(sc, sc), c2 = pack2(st.cp, st.cq);
 #pragma unroll
             for (int j = 0; j < kV; ++j) {
-              float ep, eq, p, q;
-              unpack2(fma2(pack2(masked(lt[j], st.tt), resid ? masked(ld[j], st.dt) : -INFINITY), sc2, nm2), ep,
-                      eq);
-              unpack2(mul2(pack2(fast_exp2(ep), fast_exp2(eq)), i2), p, q);
-              const float w = resid ? fmaxf(p - q, 0.f) : p;
-              sw += w;
-              spp += p;
+              float ep, eq;
+              unpack2(fma2(pack2(masked(lt[j], st.tt), masked(ld[j], st.dt)), sc2, c2), ep, eq);
+              sw += fmaxf(fast_exp2(ep) - fast_exp2(eq), 0.f);
             }
           } else {
 #pragma unroll
-            for (int j = 0; j < kV; ++j) {
-              const float p = __fmul_rn(fast_exp2(fmaf(masked(lt[j], st.tt), sc, st.nmp)), st.ip);
-              const float w =
-                  resid ? fmaxf(p - __fmul_rn(fast_exp2(fmaf(masked(ld[j], st.dt), sc, st.nmq)), st.iq), 0.f) : p;
-              sw += w;
-              spp += p;
-            }
+            for (int j = 0; j < kV; ++j)
+              sw += fmaxf(fast_exp2(fmaf(masked(lt[j], st.tt), sc, st.cp)) -
+                              fast_exp2(fmaf(masked(ld[j], st.dt), sc, st.cq)),
+                          0.f);
           }
           lw += sw;
-          lp += spp;
         }
       } else {
 #pragma unroll
@@ -618,12 +652,12 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_draw_kernel(const Sa
           float pv[kV], wv[kV];
           seg_weights<T>(tr, dr, resid, a.V, vec, c * cpc + r * seg + lane * kV, st, sc, pv, wv);
           lw += lane_sum<kV>(wv);
-          lp += lane_sum<kV>(pv);
         }
       }
+      // the chunk's weight mass (the residual, or p); the p masses of a residual row are only needed
+      // when its residual mass is degenerate, and the resolving CTA computes them then
       const float cw = warp_sum(lw);
-      const float cp = resid ? warp_sum(lp) : cw;
-      if (lane == 0) sm.cs[c - c0] = make_float2(cw, cp);
+      if (lane == 0) sm.cs[c - c0] = make_float2(cw, resid ? 0.f : cw);
     }
     __syncthreads();
     if (tid == 0) {  // slice masses: the chunk masses summed in chunk order

@@ -186,3 +186,29 @@ def test_one_hot_and_identical_rows_without_boundary_exemption(S):
     em, na = S.verify_sample(same, same[:, :gamma].contiguous(), ids, u, 1.0)
     assert (na == gamma).all()
     assert S.check_status() == 0
+
+
+@pytest.mark.parametrize("dtype,V", [("f32", 5000), ("f32", 70000), ("bf16", 40000)])
+def test_degenerate_residual_draws_from_p(S, dtype, V):
+    """R4 on the GPU: the draft token has p(x) = 0 (always rejected) and q(x) ~ 1e-17, every other logit
+    equal, so the residual max(0, p - q) has mass ~1e-17 <= 1e-15 and the draw falls back to p."""
+    B, gamma = 16, 1
+    base = 2.0 * normal_f32((B, 1, V), 71, V, "cuda")
+    t = torch.cat([base, base], dim=1).clone()
+    d = base.clone()
+    ids = torch.randint(0, V, (B, 1), generator=torch.Generator("cuda").manual_seed(3), device="cuda",
+                        dtype=torch.int32)
+    rows = torch.arange(B, device="cuda")
+    mx = base.amax(dim=2)[:, 0]
+    t[rows, 0, ids[:, 0].long()] = float("-inf")           # p(x) = 0
+    d[rows, 0, ids[:, 0].long()] = mx - 40.0               # q(x) about e^-40 of the top token
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    t, d = t.to(tdt).contiguous(), d.to(tdt).contiguous()
+    u = uniform_f32((B, gamma + 1), 72, V, "cuda")
+    w = W.Workload(name="degenerate", B=B, gamma=gamma, V=V, dtype=dtype, T=1.0, target=t, draft=d, ids=ids,
+                   uniforms=u)
+    em, na = S.verify_sample(t, d, ids, u, 1.0)
+    assert S.check_status() == 0
+    assert bool((na == 0).all())
+    n, flagged, mism = compare_sample(w, em, na)
+    assert not mism, mism[:3]
