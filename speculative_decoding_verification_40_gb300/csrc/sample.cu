@@ -210,7 +210,10 @@ __device__ void resolve_row(const SampleParams& a, int b, int gb, const RowState
   int32_t* e = a.emitted + (size_t)b * G1;
   const bool resid = st.flags & kRowResid;
   const bool failed = st.flags & kRowInvalid;
-  if (!failed && tid < ND) sm.ds[tid] = __ldcg(dsum + tid);
+  // one draw CTA per row: its chunk masses and slice mass are still in shared memory, nothing went through
+  // the workspace
+  const bool staged = ND == 1;
+  if (!failed && tid < ND && !staged) sm.ds[tid] = __ldcg(dsum + tid);
   __syncthreads();
   if (!failed && resid) {
     // a residual whose mass is degenerate (<= 1e-15) draws from p instead; the draw CTAs summed only the
@@ -232,12 +235,17 @@ __device__ void resolve_row(const SampleParams& a, int b, int gb, const RowState
           }
         }
         lp = warp_sum(lp);
-        if (lane == 0) dch[c].y = lp;
+        if (lane == 0) {
+          if (staged)
+            sm.cs[c].y = lp;
+          else
+            dch[c].y = lp;
+        }
       }
       __syncthreads();
       if (tid < ND) {
         float P = 0.f;
-        for (int c = 0; c < cps; ++c) P += __ldcg(&dch[tid * cps + c].y);
+        for (int c = 0; c < cps; ++c) P += staged ? sm.cs[c].y : __ldcg(&dch[tid * cps + c].y);
         sm.ds[tid].y = P;
       }
       __syncthreads();
@@ -284,8 +292,10 @@ __device__ void resolve_row(const SampleParams& a, int b, int gb, const RowState
   const int sd = sm.pick;
   if (sd >= 0) {
     const int c0 = sd * cps, c1 = min(c0 + cps, nc);
-    for (int c = c0 + tid; c < c1; c += kST) sm.cs[c - c0] = __ldcg(dch + (size_t)sd * cps + (c - c0));
-    __syncthreads();
+    if (!staged) {
+      for (int c = c0 + tid; c < c1; c += kST) sm.cs[c - c0] = __ldcg(dch + (size_t)sd * cps + (c - c0));
+      __syncthreads();
+    }
     if (tid == 0) {
       const bool use_p = sm.mode & 1;
       bool fallback = sm.mode & 2;
@@ -382,8 +392,10 @@ __device__ void resolve_row(const SampleParams& a, int b, int gb, const RowState
   float4* part = reinterpret_cast<float4*>(a.ws.part) + (size_t)b * G1 * NS;
   for (int k = tid; k < (gb + 1) * NS; k += kST) part[k] = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int k = tid; k < gb; k += kST) reinterpret_cast<float2*>(a.ws.xl)[(size_t)b * a.G + k] = make_float2(0.f, 0.f);
-  for (int k = tid; k < ND * cps; k += kST) dch[k] = make_float2(0.f, 0.f);
-  for (int k = tid; k < ND; k += kST) dsum[k] = make_float2(0.f, 0.f);
+  if (!staged) {
+    for (int k = tid; k < ND * cps; k += kST) dch[k] = make_float2(0.f, 0.f);
+    for (int k = tid; k < ND; k += kST) dsum[k] = make_float2(0.f, 0.f);
+  }
   if (tid == 0) {
     a.ws.ticket[b] = 0u;
     a.ws.stop[b] = 0;
@@ -665,20 +677,27 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_draw_kernel(const Sa
       float W = 0.f, P = 0.f;
       for (int c = 0; c < c1 - c0; ++c) {
         const float2 v = sm.cs[c];
-        dch[c] = v;
+        if (ND > 1) dch[c] = v;
         W += v.x;
         P += v.y;
       }
-      reinterpret_cast<float2*>(a.ws.dsum)[(size_t)b * ND + d] = make_float2(W, P);
+      if (ND > 1)
+        reinterpret_cast<float2*>(a.ws.dsum)[(size_t)b * ND + d] = make_float2(W, P);
+      else
+        sm.ds[0] = make_float2(W, P);  // the row's only draw CTA resolves from shared memory
     }
   }
   if (tid == 0) {
-    __threadfence();
-    sm.last = atomicAdd(a.ws.ticket + b, 1u) == static_cast<unsigned>(ND - 1);
+    if (ND > 1) {
+      __threadfence();
+      sm.last = atomicAdd(a.ws.ticket + b, 1u) == static_cast<unsigned>(ND - 1);
+    } else {
+      sm.last = 1;
+    }
   }
   __syncthreads();
   if (sm.last) {
-    __threadfence();
+    if (ND > 1) __threadfence();
     resolve_row<T>(a, b, gb, st, sm);
   }
 }
