@@ -39,6 +39,9 @@ constexpr float kZFloor = 1e-15f;
 // any shape.  Only the error word keeps its value until it is read.
 constexpr int kMaxSlices = 32;          // vocabulary slices per row in the sampling kernel
 constexpr int kMaxChunksPerSlice = 128; // chunks per sampling slice
+// Chunk slots of one drawn row (draw slices x chunks per slice): at most V / 512 + 128 = 640 for
+// V <= 262144, since a draw slice holds at least V / 32 elements and a chunk at least 512.
+constexpr int kMaxRowChunks = 640;
 
 struct Workspace {
   uint32_t* err;             // error word (bits above)
@@ -46,7 +49,6 @@ struct Workspace {
   unsigned long long* key;   // [B, G+1] greedy (value, index) argmax keys
   float* part;               // [B, G+1, kMaxSlices] float4 slice normalisers (m_p, S_p, m_q, S_q)
   float* xl;                 // [B, G] float2 target / draft logit at the draft token
-  float* dsum;               // [B, kMaxSlices] float2 mass of each draw slice (residual, p)
   float* dch;                // [B, chunks] float2 mass of each chunk of the drawn row(s)
   int* stop;                 // [B] early exit: 0 while row b is verifying, n + 1 once it stopped at n
 };
@@ -59,8 +61,7 @@ __host__ __device__ inline size_t chunks_per_row(int V) { return (size_t)(V + 12
 __host__ __device__ inline size_t ws_bytes_for(int B, int G, int V) {
   const size_t P = (size_t)B * (size_t)(G + 1);
   return 256 + align_up((size_t)B * 4, 256) + align_up(P * 8, 256) + align_up(P * kMaxSlices * 16, 256) +
-         align_up((size_t)B * G * 8, 256) + align_up((size_t)B * kMaxSlices * 8, 256) +
-         align_up((size_t)B * chunks_per_row(V) * 8, 256) + align_up((size_t)B * 4, 256);
+         align_up((size_t)B * G * 8, 256) + align_up((size_t)B * chunks_per_row(V) * 8, 256) + align_up((size_t)B * 4, 256);
 }
 
 inline Workspace ws_carve(void* base, int B, int G, int V) {
@@ -77,8 +78,6 @@ inline Workspace ws_carve(void* base, int B, int G, int V) {
   p += align_up(P * kMaxSlices * 16, 256);
   w.xl = reinterpret_cast<float*>(p);
   p += align_up((size_t)B * G * 8, 256);
-  w.dsum = reinterpret_cast<float*>(p);
-  p += align_up((size_t)B * kMaxSlices * 8, 256);
   w.dch = reinterpret_cast<float*>(p);
   p += align_up((size_t)B * chunks_per_row(V) * 8, 256);
   w.stop = reinterpret_cast<int*>(p);

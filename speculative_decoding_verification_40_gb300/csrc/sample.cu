@@ -46,9 +46,23 @@ enum : int { kRowInvalid = 1, kRowResid = 2 };
 struct RowState {
   int n, flags;
   uint32_t err;
+  float uf;      // the final draw's uniform (thread 0 only)
+  int x;         // draft id x_i of this thread's position i = thread index (i < gamma_b)
   float cp, cq;  // p = 2^(l log2(e)/T + cp), cp = -m_p log2(e)/T - log2 S_p; q likewise (times the lenience)
   float tt, dt;  // standardisation thresholds of the drawn target / draft row (-inf: none)
 };
+
+// p and w = max(0, p - q) (w = p unless resid) from widened logits: one FFMA and one exp2 per
+// probability; the chunk-mass pass, scalar or packed, computes exactly these.
+template <int kV>
+__device__ __forceinline__ void weights_of(const float (&lt)[kV], const float (&ld)[kV], bool resid,
+                                           const RowState& st, float sc, float (&p)[kV], float (&w)[kV]) {
+#pragma unroll
+  for (int j = 0; j < kV; ++j) {
+    p[j] = fast_exp2(fmaf(masked(lt[j], st.tt), sc, st.cp));
+    w[j] = resid ? fmaxf(p[j] - fast_exp2(fmaf(masked(ld[j], st.dt), sc, st.cq)), 0.f) : p[j];
+  }
+}
 
 // Weights of one lane's kV elements starting at `base` of the drawn row(s): p, and w = max(0, p - q)
 // for a residual draw (w = p otherwise); elements past V weigh 0.  The mass pass and the final scan
@@ -69,12 +83,7 @@ __device__ __forceinline__ void seg_weights(const T* tr, const T* dr, bool resid
       ld[j] = (resid && base + j < V) ? Elems<T>::one(dr, base + j) : -INFINITY;
     }
   }
-#pragma unroll
-  for (int j = 0; j < kV; ++j) {
-    // one FFMA and one exp2 per probability; the chunk-mass pass, scalar or packed, computes exactly these
-    p[j] = fast_exp2(fmaf(masked(lt[j], st.tt), sc, st.cp));
-    w[j] = resid ? fmaxf(p[j] - fast_exp2(fmaf(masked(ld[j], st.dt), sc, st.cq)), 0.f) : p[j];
-  }
+  weights_of<kV>(lt, ld, resid, st, sc, p, w);
 }
 
 template <int kV>
@@ -88,8 +97,8 @@ __device__ __forceinline__ float lane_sum(const float (&w)[kV]) {
 struct DrawSmem {
   float mp[kMaxGamma + 1], sp[kMaxGamma + 1], mq[kMaxGamma + 1], sq[kMaxGamma + 1];
   int acc[kMaxGamma + 1];
-  float2 cs[kMaxChunksPerSlice];  // chunk masses of this CTA's slice, then of the chosen slice (w, p)
-  float2 ds[kMaxSlices];          // slice masses of the drawn row (w, p)
+  float2 cs[kMaxRowChunks];  // chunk masses of the drawn row (w, p), gathered by the resolving CTA
+  float2 ds[kMaxSlices];     // slice masses of the drawn row (w, p)
   uint32_t err;
   int last, pick, mode;
   float t, pre;
@@ -98,10 +107,8 @@ struct DrawSmem {
 // Accept decisions of row b from the slice normalisers: the same arithmetic in every CTA of the row.
 // Row normalisers of one position from its NS slice partials (m_p, S_p, m_q, S_q), combined by one warp
 // in a fixed order, so every caller gets the same values bit for bit.  Every lane returns them.
-__device__ __forceinline__ float4 position_norm(const float4* __restrict__ part_pos, int NS, float sc) {
-  const int lane = threadIdx.x & 31;
-  float4 pr = make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
-  if (lane < NS) pr = __ldcg(part_pos + lane);
+// pr: lane r < NS holds slice r's partial (m_p, S_p, m_q, S_q), the other lanes (-inf, 0, -inf, 0).
+__device__ __forceinline__ float4 combine_partials(float4 pr, int NS, float sc) {
   const float Mp = warp_max_nan(pr.x);
   const float Mq = warp_max_nan(pr.z);
   const float tp = (pr.x > -INFINITY && Mp < INFINITY) ? pr.y * fast_exp2((pr.x - Mp) * sc) : 0.f;
@@ -114,33 +121,74 @@ __device__ __forceinline__ float4 position_norm(const float4* __restrict__ part_
   return make_float4(Mp, Sp, Mq, Sq);
 }
 
+__device__ __forceinline__ float4 load_partial(const float4* __restrict__ part_pos, int NS) {
+  float4 pr = make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+  if ((threadIdx.x & 31) < NS) pr = __ldcg(part_pos + (threadIdx.x & 31));
+  return pr;
+}
+
+__device__ __forceinline__ float4 position_norm(const float4* __restrict__ part_pos, int NS, float sc) {
+  return combine_partials(load_partial(part_pos, NS), NS, sc);
+}
+
 // Accept test of guess i < gamma_b of row b, u_i <= min(1, p(x_i)/q(x_i)) with p(x_i) > 0, from the
 // position's normalisers and the logits at the draft token; err collects what makes the row invalid.
-__device__ __forceinline__ int accept_position(const SampleParams& a, int b, int i, float4 nm, uint32_t& err) {
-  const int x = __ldg(a.ids + (size_t)b * a.G + i);
-  const float ui = __ldg(a.uniforms + (size_t)b * (a.G + 1) + i);
+// x = x_i, ui = u_i and xl = (l_p(x_i), l_q(x_i)) are passed in, so callers can load them early.
+__device__ __forceinline__ int accept_test(const SampleParams& a, float4 nm, int x, float ui, float2 xl,
+                                           uint32_t& err) {
   if (!(nm.x > -INFINITY && nm.x < INFINITY)) err |= kErrNonfinite;
   if (!(nm.z > -INFINITY && nm.z < INFINITY)) err |= kErrNonfinite;
   if (x < 0 || x >= a.V) err |= kErrToken;
   if (!(ui >= 0.f && ui < 1.f)) err |= kErrArg;
   if (err) return 0;
   const float sc = a.scale;
-  const float2 xl = __ldcg(reinterpret_cast<const float2*>(a.ws.xl) + (size_t)b * a.G + i);
   const float px = fast_exp2((xl.x - nm.x) * sc) / nm.y;
   const float qx = fast_exp2((xl.y - nm.z) * sc) / nm.w * a.lq;  // l q(x) (l = 1 unless lenient)
   const float ratio = px >= qx ? 1.f : px / qx;  // min(1, p/q); q = 0 < p gives 1
   return (px > 0.f && ui <= ratio) ? 1 : 0;
 }
 
-__device__ RowState decide_row(const SampleParams& a, int b, int gb, DrawSmem& sm) {
+__device__ __forceinline__ int accept_position(const SampleParams& a, int b, int i, float4 nm, uint32_t& err) {
+  const int x = __ldg(a.ids + (size_t)b * a.G + i);
+  const float ui = __ldg(a.uniforms + (size_t)b * (a.G + 1) + i);
+  const float2 xl = __ldcg(reinterpret_cast<const float2*>(a.ws.xl) + (size_t)b * a.G + i);
+  return accept_test(a, nm, x, ui, xl, err);
+}
+
+// Inputs of the row's decisions that the stream kernel does not write, loaded by the draw kernel before
+// it waits for the stream kernel: thread i <= gamma_b holds x_i and u_i, thread 0 also u_final.
+struct RowInputs {
+  int x;
+  float u, uf;
+};
+
+__device__ __forceinline__ RowInputs load_row_inputs(const SampleParams& a, int b, int gb) {
+  const int tid = threadIdx.x;
+  RowInputs in = {0, 0.f, 0.f};
+  if (tid < gb) in.x = __ldg(a.ids + (size_t)b * a.G + tid);
+  if (tid < gb) in.u = __ldg(a.uniforms + (size_t)b * (a.G + 1) + tid);
+  if (tid == 0) in.uf = __ldg(a.uniforms + (size_t)b * (a.G + 1) + a.G);
+  return in;
+}
+
+__device__ RowState decide_row(const SampleParams& a, int b, int gb, const RowInputs& in, DrawSmem& sm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G1 = a.G + 1;
   const int NS = a.nslices;
   const float sc = a.scale;
   const float4* part = reinterpret_cast<const float4*>(a.ws.part) + (size_t)b * G1 * NS;
-  // per-position normalisers from the slice partials (fixed combination order)
+  // the logits at the draft tokens, loaded while the warps combine the slice normalisers
+  float2 xl = make_float2(0.f, 0.f);
+  if (tid < gb) xl = __ldcg(reinterpret_cast<const float2*>(a.ws.xl) + (size_t)b * a.G + tid);
+  // per-position normalisers from the slice partials (fixed combination order); each warp loads the
+  // partials of its first two positions before combining them, one round trip for gamma_b < 2 x warps
+  const int i0 = warp, i1 = warp + kSW;
+  const float4 pr0 = i0 <= gb ? load_partial(part + (size_t)i0 * NS, NS) : make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4 pr1 = i1 <= gb ? load_partial(part + (size_t)i1 * NS, NS) : make_float4(0.f, 0.f, 0.f, 0.f);
   for (int i = warp; i <= gb; i += kSW) {
-    const float4 nm = position_norm(part + (size_t)i * NS, NS, sc);
+    const float4 nm = i == i0 ? combine_partials(pr0, NS, sc)
+                    : i == i1 ? combine_partials(pr1, NS, sc)
+                              : position_norm(part + (size_t)i * NS, NS, sc);
     if (lane == 0) {
       sm.mp[i] = nm.x;
       sm.sp[i] = nm.y;
@@ -151,22 +199,18 @@ __device__ RowState decide_row(const SampleParams& a, int b, int gb, DrawSmem& s
   if (tid == 0) sm.err = 0;
   __syncthreads();
   // validity and accept decisions, one thread per position
-  const float* U = a.uniforms + (size_t)b * G1;
   uint32_t err = 0;
   if (tid <= gb) {
     const int i = tid;
     int code = 1;
     if (i < gb) {
-      code = accept_position(a, b, i, make_float4(sm.mp[i], sm.sp[i], sm.mq[i], sm.sq[i]), err);
+      code = accept_test(a, make_float4(sm.mp[i], sm.sp[i], sm.mq[i], sm.sq[i]), in.x, in.u, xl, err);
     } else if (!(sm.mp[i] > -INFINITY && sm.mp[i] < INFINITY)) {
       err |= kErrNonfinite;
     }
     sm.acc[i] = err ? -1 : code;
   }
-  if (tid == 0) {
-    const float uf = __ldg(U + a.G);
-    if (!(uf >= 0.f && uf < 1.f)) err |= kErrArg;
-  }
+  if (tid == 0 && !(in.uf >= 0.f && in.uf < 1.f)) err |= kErrArg;
   if (err) atomicOr(&sm.err, err);
   __syncthreads();
   RowState st = {};
@@ -179,6 +223,8 @@ __device__ RowState decide_row(const SampleParams& a, int b, int gb, DrawSmem& s
   }
   st.n = n;
   st.err = sm.err;
+  st.uf = in.uf;
+  st.x = in.x;
   if (st.err) {
     st.flags = kRowInvalid;
   } else {
@@ -205,15 +251,26 @@ __device__ void resolve_row(const SampleParams& a, int b, int gb, const RowState
   const int cpc = kR * seg;
   const int cps = a.dslice / cpc;
   const int nc = (a.V + cpc - 1) / cpc;
-  float2* dsum = reinterpret_cast<float2*>(a.ws.dsum) + (size_t)b * ND;
   float2* dch = reinterpret_cast<float2*>(a.ws.dch) + (size_t)b * ND * cps;
   int32_t* e = a.emitted + (size_t)b * G1;
   const bool resid = st.flags & kRowResid;
   const bool failed = st.flags & kRowInvalid;
-  // one draw CTA per row: its chunk masses and slice mass are still in shared memory, nothing went through
-  // the workspace
+  // the chunk masses of the whole row in shared memory: already there when the row has one draw CTA,
+  // else one round trip for all of them
   const bool staged = ND == 1;
-  if (!failed && tid < ND && !staged) sm.ds[tid] = __ldcg(dsum + tid);
+  if (!failed && !staged)
+    for (int c = tid; c < ND * cps; c += kST) sm.cs[c] = __ldcg(dch + c);
+  __syncthreads();
+  // slice masses: each slice's chunk masses summed in chunk order
+  if (!failed && tid < ND) {
+    const int lo = tid * cps, hi = min(lo + cps, nc);
+    float W = 0.f, P = 0.f;
+    for (int c = lo; c < hi; ++c) {
+      W += sm.cs[c].x;
+      P += sm.cs[c].y;
+    }
+    sm.ds[tid] = make_float2(W, P);
+  }
   __syncthreads();
   if (!failed && resid) {
     // a residual whose mass is degenerate (<= 1e-15) draws from p instead; the draw CTAs summed only the
@@ -224,28 +281,22 @@ __device__ void resolve_row(const SampleParams& a, int b, int gb, const RowState
     if (!(Z > kZFloor)) {
       const int warp = tid >> 5;
       const T* tr = reinterpret_cast<const T*>(a.target) + ((size_t)b * G1 + st.n) * a.V;
-      for (int c = warp; c < ND * cps; c += kSW) {
+      for (int c = warp; c < nc; c += kSW) {
         float lp = 0.f;
-        if (c < nc) {
 #pragma unroll
-          for (int r = 0; r < kR; ++r) {
-            float pv[kV], wv[kV];
-            seg_weights<T>(tr, tr, false, a.V, a.vec != 0, c * cpc + r * seg + lane * kV, st, a.scale, pv, wv);
-            lp += lane_sum<kV>(pv);
-          }
+        for (int r = 0; r < kR; ++r) {
+          float pv[kV], wv[kV];
+          seg_weights<T>(tr, tr, false, a.V, a.vec != 0, c * cpc + r * seg + lane * kV, st, a.scale, pv, wv);
+          lp += lane_sum<kV>(pv);
         }
         lp = warp_sum(lp);
-        if (lane == 0) {
-          if (staged)
-            sm.cs[c].y = lp;
-          else
-            dch[c].y = lp;
-        }
+        if (lane == 0) sm.cs[c].y = lp;
       }
       __syncthreads();
       if (tid < ND) {
+        const int lo = tid * cps, hi = min(lo + cps, nc);
         float P = 0.f;
-        for (int c = 0; c < cps; ++c) P += staged ? sm.cs[c].y : __ldcg(&dch[tid * cps + c].y);
+        for (int c = lo; c < hi; ++c) P += sm.cs[c].y;
         sm.ds[tid].y = P;
       }
       __syncthreads();
@@ -253,7 +304,7 @@ __device__ void resolve_row(const SampleParams& a, int b, int gb, const RowState
   }
   if (!failed && tid == 0) {
     // total mass in slice order; the residual, or p when the residual mass is degenerate
-    const float uf = __ldg(a.uniforms + (size_t)b * G1 + a.G);
+    const float uf = st.uf;
     float Z = 0.f, P = 0.f;
     for (int d = 0; d < ND; ++d) {
       Z += sm.ds[d].x;
@@ -288,14 +339,10 @@ __device__ void resolve_row(const SampleParams& a, int b, int gb, const RowState
   }
   if (failed && tid == 0) sm.pick = -1;
   __syncthreads();
-  // chunk within the chosen slice: stage its chunk masses, then one thread scans them
+  // chunk within the chosen slice: one thread scans its chunk masses
   const int sd = sm.pick;
   if (sd >= 0) {
     const int c0 = sd * cps, c1 = min(c0 + cps, nc);
-    if (!staged) {
-      for (int c = c0 + tid; c < c1; c += kST) sm.cs[c - c0] = __ldcg(dch + (size_t)sd * cps + (c - c0));
-      __syncthreads();
-    }
     if (tid == 0) {
       const bool use_p = sm.mode & 1;
       bool fallback = sm.mode & 2;
@@ -303,7 +350,7 @@ __device__ void resolve_row(const SampleParams& a, int b, int gb, const RowState
       int pc = -1, lastc = -1;
       float cum2 = sm.pre, cpre = 0.f;
       for (int c = c0; c < c1; ++c) {
-        const float v = use_p ? sm.cs[c - c0].y : sm.cs[c - c0].x;
+        const float v = use_p ? sm.cs[c].y : sm.cs[c].x;
         if (v > 0.f) {
           if (!fallback && pc < 0 && cum2 + v > t) {
             pc = c;
@@ -327,14 +374,34 @@ __device__ void resolve_row(const SampleParams& a, int b, int gb, const RowState
   if (pc >= 0 && tid < 32) {  // warp 0: the token inside the chunk, segment by segment
     const bool use_p = sm.mode & 1;
     const bool fallback = sm.mode & 2;
+    const bool res = resid && !use_p;
     const T* tr = reinterpret_cast<const T*>(a.target) + ((size_t)b * G1 + st.n) * a.V;
     const T* dr = resid ? reinterpret_cast<const T*>(a.draft) + ((size_t)b * a.G + st.n) * a.V : tr;
+    // a whole chunk of aligned rows: every segment's loads issued at once (one round trip), then the scan
+    const bool vchunk = a.vec != 0 && (pc + 1) * cpc <= a.V;
+    uint4 rt[kR], rd[kR];
+    if (vchunk) {
+#pragma unroll
+      for (int r = 0; r < kR; ++r) {
+        rt[r] = ldg_stream(tr + pc * cpc + r * seg + lane * kV);
+        rd[r] = res ? ldg_stream(dr + pc * cpc + r * seg + lane * kV) : make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
     float tt = sm.t - sm.pre;
     int tok = -1, lasttok = -1;
-    for (int r = 0; r < kR && tok < 0; ++r) {
+#pragma unroll
+    for (int r = 0; r < kR; ++r) {
+      if (tok >= 0) continue;  // warp-uniform
       const int base = pc * cpc + r * seg + lane * kV;
       float pv[kV], wv[kV];
-      seg_weights<T>(tr, dr, resid && !use_p, a.V, a.vec != 0, base, st, a.scale, pv, wv);
+      if (vchunk) {
+        float lt[kV], ld[kV];
+        Elems<T>::widen(rt[r], lt);
+        Elems<T>::widen(rd[r], ld);
+        weights_of<kV>(lt, ld, res, st, a.scale, pv, wv);
+      } else {
+        seg_weights<T>(tr, dr, res, a.V, a.vec != 0, base, st, a.scale, pv, wv);
+      }
       const float ls = lane_sum<kV>(wv);
       const float inc = warp_inclusive_scan(ls, lane);
       float exc = __shfl_up_sync(0xffffffffu, inc, 1);
@@ -370,17 +437,12 @@ __device__ void resolve_row(const SampleParams& a, int b, int gb, const RowState
     }
     if (tok < 0) tok = lasttok;
     if (!bounds_ok(tok < a.V, a.ws.err)) tok = -1;
+    // the outputs, one lane per slot: the accepted drafts, the drawn token, then -1
+    for (int j = lane; j < G1; j += 32)
+      e[j] = tok < 0 ? -1 : j < st.n ? (j < 32 ? st.x : __ldg(a.ids + (size_t)b * a.G + j)) : j == st.n ? tok : -1;
     if (lane == 0) {
-      if (tok >= 0) {
-        for (int j = 0; j < st.n; ++j) e[j] = __ldg(a.ids + (size_t)b * a.G + j);
-        e[st.n] = tok;
-        for (int j = st.n + 1; j < G1; ++j) e[j] = -1;
-        a.n_acc[b] = st.n;
-      } else {  // no weight anywhere (cannot happen for a valid row): report, never index
-        for (int j = 0; j < G1; ++j) e[j] = -1;
-        a.n_acc[b] = -1;
-        atomicOr(a.ws.err, kErrNonfinite);
-      }
+      a.n_acc[b] = tok >= 0 ? st.n : -1;
+      if (tok < 0) atomicOr(a.ws.err, kErrNonfinite);  // no weight anywhere (cannot happen for a valid row)
     }
   } else if (tid == 0) {
     for (int j = 0; j < G1; ++j) e[j] = -1;
@@ -392,10 +454,8 @@ __device__ void resolve_row(const SampleParams& a, int b, int gb, const RowState
   float4* part = reinterpret_cast<float4*>(a.ws.part) + (size_t)b * G1 * NS;
   for (int k = tid; k < (gb + 1) * NS; k += kST) part[k] = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int k = tid; k < gb; k += kST) reinterpret_cast<float2*>(a.ws.xl)[(size_t)b * a.G + k] = make_float2(0.f, 0.f);
-  if (!staged) {
+  if (!staged)
     for (int k = tid; k < ND * cps; k += kST) dch[k] = make_float2(0.f, 0.f);
-    for (int k = tid; k < ND; k += kST) dsum[k] = make_float2(0.f, 0.f);
-  }
   if (tid == 0) {
     a.ws.ticket[b] = 0u;
     a.ws.stop[b] = 0;
@@ -585,6 +645,8 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_draw_kernel(const Sa
   const int d = static_cast<int>(blockIdx.x % ND);
   const int G1 = a.G + 1;
   const int gb = a.draft_len ? __ldg(a.draft_len + b) : a.G;
+  // the row's draft ids and uniforms are inputs: load them while the stream kernel drains
+  const RowInputs in = (gb >= 0 && gb <= a.G) ? load_row_inputs(a, b, gb) : RowInputs{0, 0.f, 0.f};
   // launched as a programmatic dependent of the stream kernel: wait for all of it (and its writes)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (gb < 0 || gb > a.G) {  // invalid draft length: nothing was streamed for this row
@@ -596,7 +658,7 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_draw_kernel(const Sa
     }
     return;
   }
-  const RowState st = decide_row(a, b, gb, sm);
+  const RowState st = decide_row(a, b, gb, in, sm);
   if (!(st.flags & kRowInvalid)) {
     const bool resid = st.flags & kRowResid;
     const bool vec = a.vec != 0;
@@ -607,7 +669,10 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_draw_kernel(const Sa
     const int cps = a.dslice / cpc;              // chunks per slice
     const int c0 = d * cps;
     const int c1 = min(c0 + cps, (a.V + cpc - 1) / cpc);
-    if (!bounds_ok(cps <= kMaxChunksPerSlice && (size_t)ND * cps <= chunks_per_row(a.V) && st.n <= gb, a.ws.err))
+    float2* dch = reinterpret_cast<float2*>(a.ws.dch) + (size_t)b * ND * cps;
+    if (!bounds_ok(cps <= kMaxChunksPerSlice && ND * cps <= kMaxRowChunks &&
+                       (size_t)ND * cps <= chunks_per_row(a.V) && st.n <= gb,
+                   a.ws.err))
       return;
     const float sc = a.scale;
     for (int c = c0 + warp; c < c1; c += kSW) {
@@ -667,26 +732,20 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_draw_kernel(const Sa
         }
       }
       // the chunk's weight mass (the residual, or p); the p masses of a residual row are only needed
-      // when its residual mass is degenerate, and the resolving CTA computes them then
+      // when its residual mass is degenerate, and the resolving CTA computes them then.  A row with one
+      // draw CTA keeps them in shared memory for its resolution; otherwise they go to the workspace.
       const float cw = warp_sum(lw);
-      if (lane == 0) sm.cs[c - c0] = make_float2(cw, resid ? 0.f : cw);
-    }
-    __syncthreads();
-    if (tid == 0) {  // slice masses: the chunk masses summed in chunk order
-      float2* dch = reinterpret_cast<float2*>(a.ws.dch) + ((size_t)b * ND + d) * cps;
-      float W = 0.f, P = 0.f;
-      for (int c = 0; c < c1 - c0; ++c) {
-        const float2 v = sm.cs[c];
-        if (ND > 1) dch[c] = v;
-        W += v.x;
-        P += v.y;
+      if (lane == 0) {
+        const float2 v = make_float2(cw, resid ? 0.f : cw);
+        if (ND > 1)
+          dch[c] = v;
+        else
+          sm.cs[c] = v;
       }
-      if (ND > 1)
-        reinterpret_cast<float2*>(a.ws.dsum)[(size_t)b * ND + d] = make_float2(W, P);
-      else
-        sm.ds[0] = make_float2(W, P);  // the row's only draw CTA resolves from shared memory
     }
+    if (ND > 1 && lane == 0) __threadfence();  // the chunk masses before the arrival count
   }
+  __syncthreads();  // every warp's chunk masses written (and fenced) before the arrival
   if (tid == 0) {
     if (ND > 1) {
       __threadfence();
