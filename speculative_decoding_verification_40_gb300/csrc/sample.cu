@@ -240,6 +240,26 @@ __device__ RowState decide_row(const SampleParams& a, int b, int gb, const RowIn
   return st;
 }
 
+// Slice masses of the drawn row from its chunk masses in shared memory, one warp per slice: lane l sums
+// chunks l, l + 32, ... of the slice, then a fixed butterfly over the lanes.  which: 1 = w, 2 = p, 3 = both.
+__device__ __forceinline__ void slice_sums(DrawSmem& sm, int ND, int cps, int nc, int which) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int d = warp; d < ND; d += kSW) {
+    const int lo = d * cps, hi = min(lo + cps, nc);
+    float W = 0.f, P = 0.f;
+    for (int c = lo + lane; c < hi; c += 32) {
+      W += sm.cs[c].x;
+      P += sm.cs[c].y;
+    }
+    W = warp_sum(W);
+    P = warp_sum(P);
+    if (lane == 0) {
+      if (which & 1) sm.ds[d].x = W;
+      if (which & 2) sm.ds[d].y = P;
+    }
+  }
+}
+
 // Last CTA of row b: slice, chunk and token of the draw; the row's outputs; every slot back to zero.
 template <typename T>
 __device__ void resolve_row(const SampleParams& a, int b, int gb, const RowState& st, DrawSmem& sm) {
@@ -261,16 +281,8 @@ __device__ void resolve_row(const SampleParams& a, int b, int gb, const RowState
   if (!failed && !staged)
     for (int c = tid; c < ND * cps; c += kST) sm.cs[c] = __ldcg(dch + c);
   __syncthreads();
-  // slice masses: each slice's chunk masses summed in chunk order
-  if (!failed && tid < ND) {
-    const int lo = tid * cps, hi = min(lo + cps, nc);
-    float W = 0.f, P = 0.f;
-    for (int c = lo; c < hi; ++c) {
-      W += sm.cs[c].x;
-      P += sm.cs[c].y;
-    }
-    sm.ds[tid] = make_float2(W, P);
-  }
+  // slice masses: one warp per slice, a fixed-order reduction of its chunk masses
+  if (!failed) slice_sums(sm, ND, cps, nc, 3);
   __syncthreads();
   if (!failed && resid) {
     // a residual whose mass is degenerate (<= 1e-15) draws from p instead; the draw CTAs summed only the
@@ -293,12 +305,7 @@ __device__ void resolve_row(const SampleParams& a, int b, int gb, const RowState
         if (lane == 0) sm.cs[c].y = lp;
       }
       __syncthreads();
-      if (tid < ND) {
-        const int lo = tid * cps, hi = min(lo + cps, nc);
-        float P = 0.f;
-        for (int c = lo; c < hi; ++c) P += sm.cs[c].y;
-        sm.ds[tid].y = P;
-      }
+      slice_sums(sm, ND, cps, nc, 2);
       __syncthreads();
     }
   }
@@ -339,34 +346,57 @@ __device__ void resolve_row(const SampleParams& a, int b, int gb, const RowState
   }
   if (failed && tid == 0) sm.pick = -1;
   __syncthreads();
-  // chunk within the chosen slice: one thread scans its chunk masses
+  // chunk within the chosen slice, by warp 0: each lane takes a run of consecutive chunks, a warp scan
+  // gives the mass before each run, and the first chunk whose running mass passes t is the pick (the
+  // last chunk of positive mass if rounding leaves t beyond the slice, or if the slice pick fell back)
   const int sd = sm.pick;
   if (sd >= 0) {
-    const int c0 = sd * cps, c1 = min(c0 + cps, nc);
-    if (tid == 0) {
+    if (tid < 32) {
+      const int c0 = sd * cps, c1 = min(c0 + cps, nc);
       const bool use_p = sm.mode & 1;
-      bool fallback = sm.mode & 2;
+      const bool fb = sm.mode & 2;
       const float t = sm.t;
-      int pc = -1, lastc = -1;
-      float cum2 = sm.pre, cpre = 0.f;
-      for (int c = c0; c < c1; ++c) {
+      const int m = (cps + 31) / 32;
+      const int r0 = c0 + lane * m, r1 = min(r0 + m, c1);
+      float ls = 0.f;
+      int lpos = -1;
+      for (int c = r0; c < r1; ++c) {
         const float v = use_p ? sm.cs[c].y : sm.cs[c].x;
-        if (v > 0.f) {
-          if (!fallback && pc < 0 && cum2 + v > t) {
-            pc = c;
-            cpre = cum2;
+        ls += v;
+        if (v > 0.f) lpos = c;
+      }
+      const float inc = warp_inclusive_scan(ls, lane);
+      float cum = __shfl_up_sync(0xffffffffu, inc, 1);
+      cum = sm.pre + (lane == 0 ? 0.f : cum);
+      int hitc = -1;
+      float hpre = 0.f;
+      if (!fb) {
+        for (int c = r0; c < r1; ++c) {
+          const float v = use_p ? sm.cs[c].y : sm.cs[c].x;
+          if (v > 0.f && cum + v > t) {
+            hitc = c;
+            hpre = cum;
+            break;
           }
-          lastc = c;
+          cum += v;
         }
-        cum2 += v;
       }
-      if (pc < 0) {
-        pc = lastc;
-        fallback = true;
+      const unsigned hit = __ballot_sync(0xffffffffu, hitc >= 0);
+      const unsigned pos = __ballot_sync(0xffffffffu, lpos >= 0);
+      int pc = -1;
+      float cpre = 0.f;
+      if (hit) {
+        const int l = __ffs(hit) - 1;
+        pc = __shfl_sync(0xffffffffu, hitc, l);
+        cpre = __shfl_sync(0xffffffffu, hpre, l);
+      } else if (pos) {
+        pc = __shfl_sync(0xffffffffu, lpos, 31 - __clz(pos));
       }
-      sm.pick = pc;
-      sm.mode = (use_p ? 1 : 0) | (fallback ? 2 : 0);
-      sm.pre = cpre;
+      if (lane == 0) {
+        sm.pick = pc;
+        sm.mode = (use_p ? 1 : 0) | (hit ? 0 : 2);
+        sm.pre = cpre;
+      }
     }
     __syncthreads();
   }
