@@ -40,6 +40,7 @@ namespace {
 constexpr int kST = kStreamThreads;
 constexpr int kSW = kST / 32;
 constexpr int kR = 4;  // 16-byte vectors per lane in one draw chunk
+constexpr int kShortRowBytes = 8192;  // rows up to this size take the one-launch path
 
 enum : int { kRowInvalid = 1, kRowResid = 2 };
 
@@ -665,20 +666,15 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_stream_kernel(const 
 
 // ----------------------------------------------------------------------------- draw kernel
 
+// Draw slice d of batch row b once the row's slice normalisers are in the workspace: decisions, chunk
+// masses of the drawn row(s) in this slice, and the row's resolution in its last draw CTA.
 template <typename T>
-__global__ void __launch_bounds__(kStreamThreads, 4) verify_draw_kernel(const SampleParams a) {
-  __shared__ DrawSmem sm;
+__device__ __forceinline__ void draw_slice_of_row(const SampleParams& a, int b, int d, int gb, const RowInputs& in,
+                                                  DrawSmem& sm) {
   constexpr int kV = Elems<T>::kVec;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int ND = a.ndslices;
-  const int b = a.B - 1 - static_cast<int>(blockIdx.x / ND);  // last-streamed rows first: still in L2
-  const int d = static_cast<int>(blockIdx.x % ND);
   const int G1 = a.G + 1;
-  const int gb = a.draft_len ? __ldg(a.draft_len + b) : a.G;
-  // the row's draft ids and uniforms are inputs: load them while the stream kernel drains
-  const RowInputs in = (gb >= 0 && gb <= a.G) ? load_row_inputs(a, b, gb) : RowInputs{0, 0.f, 0.f};
-  // launched as a programmatic dependent of the stream kernel: wait for all of it (and its writes)
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (gb < 0 || gb > a.G) {  // invalid draft length: nothing was streamed for this row
     if (d == 0 && tid == 0) {
       int32_t* e = a.emitted + (size_t)b * G1;
@@ -789,6 +785,111 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_draw_kernel(const Sa
     if (ND > 1) __threadfence();
     resolve_row<T>(a, b, gb, st, sm);
   }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kStreamThreads, 4) verify_draw_kernel(const SampleParams a) {
+  __shared__ DrawSmem sm;
+  const int ND = a.ndslices;
+  const int b = a.B - 1 - static_cast<int>(blockIdx.x / ND);  // last-streamed rows first: still in L2
+  const int d = static_cast<int>(blockIdx.x % ND);
+  const int gb = a.draft_len ? __ldg(a.draft_len + b) : a.G;
+  // the row's draft ids and uniforms are inputs: load them while the stream kernel drains
+  const RowInputs in = (gb >= 0 && gb <= a.G) ? load_row_inputs(a, b, gb) : RowInputs{0, 0.f, 0.f};
+  // launched as a programmatic dependent of the stream kernel: wait for all of it (and its writes)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  draw_slice_of_row<T>(a, b, d, gb, in, sm);
+}
+
+// ----------------------------------------------------------------------------- short rows, one launch
+
+// Rows of at most kShortRowBytes (one stream slice and one draw slice per row): the whole step in one
+// CTA per batch row and one launch.  Warp w computes the normalisers of positions w, w + 8, ... over
+// the whole row (16-byte loads, four per lane and row in flight, the online softmax of the
+// stream pass, then a butterfly merge over the lanes) and writes them to the workspace as slice 0;
+// after a barrier the CTA runs the draw code above (one draw slice: decisions, chunk masses, resolution
+// from shared memory).  For short rows the step is latency-bound, and one launch and one CTA per row
+// remove the second launch and the round trip between the two kernels.
+template <typename T, bool kMask>
+__global__ void __launch_bounds__(kStreamThreads, 4) verify_short_kernel(const SampleParams a) {
+  __shared__ DrawSmem sm;
+  constexpr int kV = Elems<T>::kVec;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int b = blockIdx.x;
+  const int G1 = a.G + 1;
+  const int gb = a.draft_len ? __ldg(a.draft_len + b) : a.G;
+  const bool valid = gb >= 0 && gb <= a.G;
+  const RowInputs in = valid ? load_row_inputs(a, b, gb) : RowInputs{0, 0.f, 0.f};
+  const float sc = a.scale;
+  const int nv = a.V / kV;  // whole vectors of the row (rows are 16-byte aligned here)
+  if (valid && bounds_ok(a.nslices == 1 && a.ndslices == 1, a.ws.err)) {
+    for (int i = warp; i <= gb; i += kSW) {
+      const bool has_q = i < gb;
+      const T* tp = reinterpret_cast<const T*>(a.target) + ((size_t)b * G1 + i) * a.V;
+      const T* dp = has_q ? reinterpret_cast<const T*>(a.draft) + ((size_t)b * a.G + i) * a.V : tp;
+      const float tt = kMask && a.tthr ? __ldg(a.tthr + (size_t)b * G1 + i) : -INFINITY;
+      const float dt = kMask && has_q && a.dthr ? __ldg(a.dthr + (size_t)b * a.G + i) : -INFINITY;
+      float mp = -INFINITY, sp = 0.f, rp = -INFINITY, mq = -INFINITY, sq = 0.f, rq = -INFINITY;
+      for (int v0 = 0; v0 < nv; v0 += 4 * 32) {  // four vectors per lane and row in flight
+        uint4 rt[4], rd[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int v = v0 + lane + 32 * u;
+          if (v < nv) {
+            rt[u] = ldg_stream(reinterpret_cast<const uint4*>(tp) + v);
+            if (has_q) rd[u] = ldg_stream(reinterpret_cast<const uint4*>(dp) + v);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (v0 + lane + 32 * u < nv) {
+            const uint4 r1[1] = {rt[u]};
+            online_group<T, 1, kMask>(mp, sp, rp, r1, sc, tt);
+            if (has_q) {
+              const uint4 q1[1] = {rd[u]};
+              online_group<T, 1, kMask>(mq, sq, rq, q1, sc, dt);
+            }
+          }
+        }
+      }
+      for (int k = nv * kV + lane; k < a.V; k += 32) {  // elements past the last whole vector
+        float f[1] = {Elems<T>::one(tp, k)};
+        online<1, kMask>(mp, sp, rp, f, sc, tt);
+        if (has_q) {
+          f[0] = Elems<T>::one(dp, k);
+          online<1, kMask>(mq, sq, rq, f, sc, dt);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float om = __shfl_xor_sync(0xffffffffu, mp, o), os = __shfl_xor_sync(0xffffffffu, sp, o);
+        const float qm = __shfl_xor_sync(0xffffffffu, mq, o), qs = __shfl_xor_sync(0xffffffffu, sq, o);
+        merge(mp, sp, om, os, sc);
+        merge(mq, sq, qm, qs, sc);
+      }
+      rp = warp_max_nan(max_nan(rp, rq));
+      if (lane == 0) {
+        const bool bad = !(rp < INFINITY);  // NaN or +inf in the row
+        reinterpret_cast<float4*>(a.ws.part)[(size_t)b * G1 + i] =
+            make_float4(bad ? NAN : mp, sp, bad ? NAN : mq, sq);
+        if (has_q) {  // the logits at the draft token
+          const int x = __ldg(a.ids + (size_t)b * a.G + i);
+          if (x >= 0 && x < a.V)
+            reinterpret_cast<float2*>(a.ws.xl)[(size_t)b * a.G + i] =
+                make_float2(masked(Elems<T>::one(tp, x), tt), masked(Elems<T>::one(dp, x), dt));
+        }
+      }
+    }
+  }
+  __syncthreads();  // the normalisers in the workspace are visible to the whole CTA
+  draw_slice_of_row<T>(a, b, 0, gb, in, sm);
+}
+
+// The one-launch path applies to 16-byte aligned rows of at most kShortRowBytes with one stream slice and
+// one draw slice per row.
+static bool short_rows(const SampleParams& p, size_t esz) {
+  return p.vec != 0 && p.step == 0 && static_cast<size_t>(p.V) * esz <= static_cast<size_t>(kShortRowBytes) &&
+         p.nslices == 1 && p.ndslices == 1;
 }
 
 template <typename T>
@@ -1189,6 +1290,10 @@ cudaError_t rows_sample_launch(const SampleParams& p, int dtype, cudaStream_t st
 template <typename T, bool kMask>
 static cudaError_t sample_launch_t(const SampleParams& p, int phases, cudaStream_t stream) {
   const dim3 block(kStreamThreads);
+  if (phases == 3 && short_rows(p, sizeof(T))) {
+    verify_short_kernel<T, kMask><<<dim3(static_cast<unsigned>(p.B)), block, 0, stream>>>(p);
+    return cudaGetLastError();
+  }
   const dim3 g1(static_cast<unsigned>((long long)p.B * (p.G + 1) * p.nslices));
   if (phases & 1) {
     verify_stream_kernel<T, kMask><<<g1, block, 0, stream>>>(p);
