@@ -63,8 +63,8 @@ typedef enum {
 
 /* Bytes of device workspace the entry points need for (B, gamma, V): an error
  * word, per-row arrival counters, greedy argmax keys, per-slice softmax
- * normalisers, the logits at the draft tokens, and the slice and chunk masses
- * of the drawn rows.  The workspace must be zero-filled once before its first
+ * normalisers, the logits at the draft tokens, the chunk masses of the drawn
+ * rows, and the early exit's stop positions.  The workspace must be zero-filled once before its first
  * use (cudaMemset or spec_workspace_init); every call leaves the slots it used
  * at zero again, so one workspace serves any sequence of calls of any shape on
  * one stream.  Calls that overlap on the GPU must use different workspaces.
