@@ -98,6 +98,7 @@ __device__ __forceinline__ float lane_sum(const float (&w)[kV]) {
 struct DrawSmem {
   float mp[kMaxGamma + 1], sp[kMaxGamma + 1], mq[kMaxGamma + 1], sq[kMaxGamma + 1];
   int acc[kMaxGamma + 1];
+  float2 xl[kMaxGamma];  // logits at the draft tokens (short-row path)
   float2 cs[kMaxRowChunks];  // chunk masses of the drawn row (w, p), gathered by the resolving CTA
   float2 ds[kMaxSlices];     // slice masses of the drawn row (w, p)
   uint32_t err;
@@ -172,29 +173,36 @@ __device__ __forceinline__ RowInputs load_row_inputs(const SampleParams& a, int 
   return in;
 }
 
-__device__ RowState decide_row(const SampleParams& a, int b, int gb, const RowInputs& in, DrawSmem& sm) {
+// staged: the caller already put the row normalisers in sm.mp .. sm.sq and the logits at the draft
+// tokens in sm.xl (the short-row path); otherwise they are combined from the workspace here.
+__device__ RowState decide_row(const SampleParams& a, int b, int gb, const RowInputs& in, DrawSmem& sm,
+                               bool staged = false) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G1 = a.G + 1;
   const int NS = a.nslices;
   const float sc = a.scale;
-  const float4* part = reinterpret_cast<const float4*>(a.ws.part) + (size_t)b * G1 * NS;
-  // the logits at the draft tokens, loaded while the warps combine the slice normalisers
   float2 xl = make_float2(0.f, 0.f);
-  if (tid < gb) xl = __ldcg(reinterpret_cast<const float2*>(a.ws.xl) + (size_t)b * a.G + tid);
-  // per-position normalisers from the slice partials (fixed combination order); each warp loads the
-  // partials of its first two positions before combining them, one round trip for gamma_b < 2 x warps
-  const int i0 = warp, i1 = warp + kSW;
-  const float4 pr0 = i0 <= gb ? load_partial(part + (size_t)i0 * NS, NS) : make_float4(0.f, 0.f, 0.f, 0.f);
-  const float4 pr1 = i1 <= gb ? load_partial(part + (size_t)i1 * NS, NS) : make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int i = warp; i <= gb; i += kSW) {
-    const float4 nm = i == i0 ? combine_partials(pr0, NS, sc)
-                    : i == i1 ? combine_partials(pr1, NS, sc)
-                              : position_norm(part + (size_t)i * NS, NS, sc);
-    if (lane == 0) {
-      sm.mp[i] = nm.x;
-      sm.sp[i] = nm.y;
-      sm.mq[i] = nm.z;
-      sm.sq[i] = nm.w;
+  if (staged) {
+    if (tid < gb) xl = sm.xl[tid];
+  } else {
+    const float4* part = reinterpret_cast<const float4*>(a.ws.part) + (size_t)b * G1 * NS;
+    // the logits at the draft tokens, loaded while the warps combine the slice normalisers
+    if (tid < gb) xl = __ldcg(reinterpret_cast<const float2*>(a.ws.xl) + (size_t)b * a.G + tid);
+    // per-position normalisers from the slice partials (fixed combination order); each warp loads the
+    // partials of its first two positions before combining them, one round trip for gamma_b < 2 x warps
+    const int i0 = warp, i1 = warp + kSW;
+    const float4 pr0 = i0 <= gb ? load_partial(part + (size_t)i0 * NS, NS) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 pr1 = i1 <= gb ? load_partial(part + (size_t)i1 * NS, NS) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = warp; i <= gb; i += kSW) {
+      const float4 nm = i == i0 ? combine_partials(pr0, NS, sc)
+                      : i == i1 ? combine_partials(pr1, NS, sc)
+                                : position_norm(part + (size_t)i * NS, NS, sc);
+      if (lane == 0) {
+        sm.mp[i] = nm.x;
+        sm.sp[i] = nm.y;
+        sm.mq[i] = nm.z;
+        sm.sq[i] = nm.w;
+      }
     }
   }
   if (tid == 0) sm.err = 0;
@@ -670,7 +678,7 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_stream_kernel(const 
 // masses of the drawn row(s) in this slice, and the row's resolution in its last draw CTA.
 template <typename T>
 __device__ __forceinline__ void draw_slice_of_row(const SampleParams& a, int b, int d, int gb, const RowInputs& in,
-                                                  DrawSmem& sm) {
+                                                  DrawSmem& sm, bool staged = false) {
   constexpr int kV = Elems<T>::kVec;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int ND = a.ndslices;
@@ -684,7 +692,7 @@ __device__ __forceinline__ void draw_slice_of_row(const SampleParams& a, int b, 
     }
     return;
   }
-  const RowState st = decide_row(a, b, gb, in, sm);
+  const RowState st = decide_row(a, b, gb, in, sm, staged);
   if (!(st.flags & kRowInvalid)) {
     const bool resid = st.flags & kRowResid;
     const bool vec = a.vec != 0;
@@ -806,9 +814,9 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_draw_kernel(const Sa
 // Rows of at most kShortRowBytes (one stream slice and one draw slice per row): the whole step in one
 // CTA per batch row and one launch.  Warp w computes the normalisers of positions w, w + 8, ... over
 // the whole row (16-byte loads, four per lane and row in flight, the online softmax of the
-// stream pass, then a butterfly merge over the lanes) and writes them to the workspace as slice 0;
-// after a barrier the CTA runs the draw code above (one draw slice: decisions, chunk masses, resolution
-// from shared memory).  For short rows the step is latency-bound, and one launch and one CTA per row
+// stream pass, then a butterfly merge over the lanes) into shared memory; after a barrier the CTA runs
+// the draw code above on them (one draw slice: decisions, chunk masses, resolution, all from shared
+// memory).  For short rows the step is latency-bound, and one launch and one CTA per row
 // remove the second launch and the round trip between the two kernels.
 template <typename T, bool kMask>
 __global__ void __launch_bounds__(kStreamThreads, 4) verify_short_kernel(const SampleParams a) {
@@ -870,19 +878,20 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_short_kernel(const S
       rp = warp_max_nan(max_nan(rp, rq));
       if (lane == 0) {
         const bool bad = !(rp < INFINITY);  // NaN or +inf in the row
-        reinterpret_cast<float4*>(a.ws.part)[(size_t)b * G1 + i] =
-            make_float4(bad ? NAN : mp, sp, bad ? NAN : mq, sq);
-        if (has_q) {  // the logits at the draft token
+        sm.mp[i] = bad ? NAN : mp;
+        sm.sp[i] = sp;
+        sm.mq[i] = bad ? NAN : mq;
+        sm.sq[i] = sq;
+        if (has_q) {  // the logits at the draft token (an id outside [0, V) is reported by the accept test)
           const int x = __ldg(a.ids + (size_t)b * a.G + i);
-          if (x >= 0 && x < a.V)
-            reinterpret_cast<float2*>(a.ws.xl)[(size_t)b * a.G + i] =
-                make_float2(masked(Elems<T>::one(tp, x), tt), masked(Elems<T>::one(dp, x), dt));
+          sm.xl[i] = (x >= 0 && x < a.V) ? make_float2(masked(Elems<T>::one(tp, x), tt), masked(Elems<T>::one(dp, x), dt))
+                                         : make_float2(0.f, 0.f);
         }
       }
     }
   }
-  __syncthreads();  // the normalisers in the workspace are visible to the whole CTA
-  draw_slice_of_row<T>(a, b, 0, gb, in, sm);
+  __syncthreads();  // the normalisers in shared memory
+  draw_slice_of_row<T>(a, b, 0, gb, in, sm, true);
 }
 
 // The one-launch path applies to 16-byte aligned rows of at most kShortRowBytes with one stream slice and
