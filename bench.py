@@ -489,6 +489,8 @@ def run_ours(a, rank, world, dist):
                         workspace=ws)
         assert S.check_status(ws) == 0
         line["cpu_baseline"] = cpu_oracle_rate(w, a.cpu_rows, os.cpu_count() or 1, gpu=(em, na))
+        one = cpu_oracle_rate(w, 16, 1)   # the same oracle on one core, a smaller sample
+        line["cpu_baseline"]["single_core"] = {"value": one["value"], "unit": UNIT, "sample": one["sample"]}
     return line
 
 
