@@ -115,12 +115,6 @@ __device__ __forceinline__ uint32_t dsmem_map(uint32_t addr, uint32_t rank) {
   return r;
 }
 
-__device__ __forceinline__ float dsmem_ld_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
-}
-
 // 16-byte streaming load of read-only data: no L1 allocation.
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   uint4 r;
@@ -128,47 +122,6 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
       : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
       : "l"(p));
   return r;
-}
-
-// mbarrier and bulk-copy (TMA) helpers.  Every wait is bounded: it gives up after `limit` polls.
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-// Makes mbarrier initialisations visible to the asynchronous (bulk-copy) proxy.
-__device__ __forceinline__ void mbar_init_fence() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-// Global -> this CTA's shared memory, `bytes` (a multiple of 16, both addresses 16-byte aligned),
-// completing on mbarrier `bar`.
-__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-               ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
-}
-
-// Orders this thread's earlier shared-memory accesses before later bulk-copy (async proxy) accesses.
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// Waits for the barrier's phase with the given parity to complete; false if it did not within `limit` polls.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit) {
-  for (uint32_t it = 0; it < limit; ++it) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    if (done) return true;
-  }
-  return false;
 }
 
 // Index check of debug-bounds builds (-DSPEC_DEBUG_BOUNDS): a false condition records kErrBounds in the
