@@ -531,11 +531,26 @@ __device__ __forceinline__ void slice_normalisers(const T* __restrict__ tp, cons
         online_group<T, U, kMask>(mp, sp, rp, r0, sc, tt);
         online_group<T, U, kMask>(mq, sq, rq, r1, sc, dt);
       }
-      for (; v < nv; v += kST) {
-        const uint4 r0[1] = {ldg_stream(t4 + v)};
-        const uint4 r1[1] = {ldg_stream(d4 + v)};
-        online_group<T, 1, kMask>(mp, sp, rp, r0, sc, tt);
-        online_group<T, 1, kMask>(mq, sq, rq, r1, sc, dt);
+      if constexpr (sizeof(T) == 2) {
+        // bfloat16: the thread's last (at most U - 1) vectors as one group whose missing vectors read as
+        // -inf, so all of their loads are in flight at once (a 64 KB row of 4000 vectors leaves three)
+        if (v < nv) {
+          const uint4 ninf = make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+          uint4 r0[U], r1[U];
+#pragma unroll
+          for (int u = 0; u < U; ++u) r0[u] = v + u * kST < nv ? ldg_stream(t4 + v + u * kST) : ninf;
+#pragma unroll
+          for (int u = 0; u < U; ++u) r1[u] = v + u * kST < nv ? ldg_stream(d4 + v + u * kST) : ninf;
+          online_group<T, U, kMask>(mp, sp, rp, r0, sc, tt);
+          online_group<T, U, kMask>(mq, sq, rq, r1, sc, dt);
+        }
+      } else {
+        for (; v < nv; v += kST) {
+          const uint4 r0[1] = {ldg_stream(t4 + v)};
+          const uint4 r1[1] = {ldg_stream(d4 + v)};
+          online_group<T, 1, kMask>(mp, sp, rp, r0, sc, tt);
+          online_group<T, 1, kMask>(mq, sq, rq, r1, sc, dt);
+        }
       }
     } else {
       for (; v + (U - 1) * kST < nv; v += U * kST) {
@@ -544,9 +559,19 @@ __device__ __forceinline__ void slice_normalisers(const T* __restrict__ tp, cons
         for (int u = 0; u < U; ++u) r0[u] = ldg_stream(t4 + v + u * kST);
         online_group<T, U, kMask>(mp, sp, rp, r0, sc, tt);
       }
-      for (; v < nv; v += kST) {
-        const uint4 r0[1] = {ldg_stream(t4 + v)};
-        online_group<T, 1, kMask>(mp, sp, rp, r0, sc, tt);
+      if constexpr (sizeof(T) == 2) {
+        if (v < nv) {
+          const uint4 ninf = make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+          uint4 r0[U];
+#pragma unroll
+          for (int u = 0; u < U; ++u) r0[u] = v + u * kST < nv ? ldg_stream(t4 + v + u * kST) : ninf;
+          online_group<T, U, kMask>(mp, sp, rp, r0, sc, tt);
+        }
+      } else {
+        for (; v < nv; v += kST) {
+          const uint4 r0[1] = {ldg_stream(t4 + v)};
+          online_group<T, 1, kMask>(mp, sp, rp, r0, sc, tt);
+        }
       }
     }
     done = nv * kV;
