@@ -423,6 +423,11 @@ def run_ours(a, rank, world, dist):
                                                     emitted=em, n_accepted=na, workspace=ws, target_thr=tthr,
                                                     draft_thr=dthr), max(10, a.steps), 3, stream)
     S.check_status(ws, raise_on_error=False)        # padded draft rows (NaN) have NaN thresholds: never read
+    # lenient verification (q scaled by l = 0.5 in the accept test and the residual) on the same batch
+    lenient_ms = time_device(lambda: S.verify_sample(*logits(), w.ids, w.uniforms, w.T, w.draft_len, emitted=em,
+                                                     n_accepted=na, workspace=ws, lenience=0.5),
+                             max(10, a.steps), 3, stream)
+    S.check_status(ws)
     s_logits, s_u = W.sampler_rows(w)               # the draft-side sampler over every draft row
     sampler_ms = time_device(lambda: S.sample_rows(s_logits, s_u, w.T), max(10, a.steps), 3, stream)
     esz = 4 if w.dtype == "f32" else 2
@@ -501,6 +506,7 @@ def run_ours(a, rank, world, dist):
                      "topk50_thresholds_ms": topk_ms, "topp09_thresholds_ms": topp_ms,
                      "thresholds_GB_per_s": (w.B * (2 * w.gamma + 1)) * w.V * esz / (topp_ms * 1e-3) / 1e9,
                      "masked_verify_ms_per_call": masked_ms,
+                     "lenient_verify_ms_per_call": lenient_ms,
                      "early_exit_ms_per_call": early_ms,
                      "early_exit_rows_read": early_rows, "all_positions_rows_read": w.B + 2 * pos,
                      "early_exit_GB_per_s": early_rows * w.V * esz / (early_ms * 1e-3) / 1e9,

@@ -1,5 +1,6 @@
 """bench.py's host-side contract, without a GPU: the reference arm's JSON line, the CPU-baseline parity count,
-and the rule that the recorded DRAM traffic is only reported for the kernel sources it was taken on."""
+the rule that the recorded DRAM traffic is only reported for the kernel sources it was taken on, and the
+logit copies the timed steps take in turn."""
 from __future__ import annotations
 
 import json
@@ -60,3 +61,14 @@ def test_recorded_traffic_follows_the_sources_digest(tmp_path, monkeypatch):
     assert bench.recorded_traffic("c2") is None
     f.write_text("sources_digest: 0000000000000000\nc3_bytes_per_launch: 1234\n")
     assert bench.recorded_traffic("c3") is None
+
+
+def test_rotation_gives_distinct_copies_of_the_same_logits():
+    w = W.make(0, device="cpu")
+    copies = bench.rotation(w)
+    assert len(copies) == 3
+    assert copies[0][0] is w.target and copies[0][1] is w.draft
+    ptrs = {t.data_ptr() for t, _ in copies} | {d.data_ptr() for _, d in copies}
+    assert len(ptrs) == 6                       # six separate buffers: no step re-reads another's memory
+    for t, d in copies[1:]:
+        assert t.equal(w.target) and d.equal(w.draft)
