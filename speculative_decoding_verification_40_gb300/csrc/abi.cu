@@ -72,12 +72,25 @@ int prepare(int dtype) {
   return SPEC_OK;
 }
 
+int device_sms();
+
+// Fewest vocabulary elements a stream or draw CTA is given when a small batch halves the slices.
+constexpr int kMinSlice = 4096;
+
 // Vocabulary elements per sampling CTA and logit row: 64 KB of the row, at least V/32 so a row has
-// at most 32 slices; SPECVERIFY_SLICE (elements) overrides within the same limits.
-int sample_slice(int V, int dtype) {
+// at most 32 slices.  `positions` > 0 (the verification's B (gamma + 1)): a batch that would give
+// fewer than two stream CTAs per SM has its slices halved, down to kMinSlice elements, so that a
+// latency-bound small batch still spreads over the GPU (c1, B = 8 and gamma = 4 over V = 32128:
+// 320 CTAs of 4096 elements instead of 40 of 32768).  SPECVERIFY_SLICE (elements) overrides within the
+// same limits.
+int sample_slice(int V, int dtype, long long positions = 0) {
   const int chunk = 4 * 32 * (dtype == SPEC_F32 ? 4 : 8);  // elements per draw chunk (4 x 32 lanes x 16 B)
   const int esz = dtype == SPEC_F32 ? 4 : 2;
   int slice = specv::kStreamSliceBytes / esz;
+  if (positions > 0) {
+    const long long want = 2LL * (device_sms() > 0 ? device_sms() : 152);
+    while (slice / 2 >= kMinSlice && positions * ((V + slice - 1) / slice) < want) slice /= 2;
+  }
   if (const char* env = std::getenv("SPECVERIFY_SLICE")) {
     const int want = std::atoi(env);
     if (want > 0) slice = want;
@@ -167,14 +180,17 @@ int device_sms() {
 }
 
 // Vocabulary elements per draw CTA.  A draw CTA re-reads its slice of one row only if that row
-// draws there, so wide slices cost little traffic; they are halved (32768 -> 16384) only when the
-// batch would otherwise give fewer than three draw CTAs per SM.  At least V/32 (at most 32 draw CTAs
-// per row), a multiple of the draw chunk; SPECVERIFY_DSLICE (elements) overrides within the limits.
+// draws there, so wide slices cost little traffic; they are halved (32768 -> 16384) when the batch
+// would otherwise give fewer than three draw CTAs per SM, and halved further, down to kMinSlice, while
+// it gives fewer than two (small, latency-bound batches).  At least V/32 (at most 32 draw CTAs per
+// row), a multiple of the draw chunk; SPECVERIFY_DSLICE (elements) overrides within the limits.
 int draw_slice(int B, int V, int dtype) {
   const int chunk = 4 * 32 * (dtype == SPEC_F32 ? 4 : 8);
   const long long wide = 32768;
   const long long ctas = static_cast<long long>(B) * ((V + wide - 1) / wide);
   int slice = ctas >= 3LL * device_sms() ? 32768 : 16384;
+  const long long want = 2LL * (device_sms() > 0 ? device_sms() : 152);
+  while (slice / 2 >= kMinSlice && static_cast<long long>(B) * ((V + slice - 1) / slice) < want) slice /= 2;
   if (const char* env = std::getenv("SPECVERIFY_DSLICE")) {
     const int want = std::atoi(env);
     if (want > 0) slice = want;
@@ -204,6 +220,16 @@ int early_exit_slice(int B, int V, int dtype) {
   if (slice < lo) slice = lo;
   slice = static_cast<int>(align_up(slice, chunk));
   if (slice > specv::kMaxChunksPerSlice * chunk) slice = specv::kMaxChunksPerSlice * chunk;
+  return slice;
+}
+
+// Target elements per greedy CTA: kGreedySlice, halved (down to 2048) while the batch would give fewer
+// than two CTAs per SM, as for the sampling slices.
+int greedy_slice(int B, int gamma, int V) {
+  int slice = specv::kGreedySlice;
+  const long long want = 2LL * (device_sms() > 0 ? device_sms() : 152);
+  const long long positions = static_cast<long long>(B) * (gamma + 1);
+  while (slice / 2 >= 2048 && positions * ((V + slice - 1) / slice) < want) slice /= 2;
   return slice;
 }
 
@@ -266,7 +292,7 @@ int run_verify(const void* target, const void* draft, int dtype, const int32_t* 
     p.B = B;
     p.G = gamma;
     p.V = V;
-    p.slice = sample_slice(V, dtype);
+    p.slice = sample_slice(V, dtype, static_cast<long long>(B) * (gamma + 1));
     p.nslices = (V + p.slice - 1) / p.slice;
     p.dslice = draw_slice(B, V, dtype);
     p.ndslices = (V + p.dslice - 1) / p.dslice;
@@ -464,7 +490,7 @@ int spec_verify_greedy(const void* target_logits, const void* draft_logits, int 
   p.B = B;
   p.G = gamma;
   p.V = V;
-  p.slice = specv::kGreedySlice;
+  p.slice = greedy_slice(B, gamma, V);
   p.nslices = (V + p.slice - 1) / p.slice;
   p.vec = rows_aligned(target_logits, V, esz) ? 1 : 0;
   p.emitted = emitted;
@@ -507,7 +533,10 @@ int spec_verify_plan(int B, int gamma, int V, int dtype, int* cluster_size, int*
   if (cluster_size) *cluster_size = plan.cs;
   if (slice_len) *slice_len = plan.L;
   if (smem_bytes) *smem_bytes = plan.smem;
-  if (greedy_ctas_per_row) *greedy_ctas_per_row = (V + specv::kGreedySlice - 1) / specv::kGreedySlice;
+  if (greedy_ctas_per_row) {
+    const int gs = greedy_slice(B, gamma, V);
+    *greedy_ctas_per_row = (V + gs - 1) / gs;
+  }
   return SPEC_OK;
 }
 
