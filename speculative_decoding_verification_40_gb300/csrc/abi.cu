@@ -296,6 +296,7 @@ int run_verify(const void* target, const void* draft, int dtype, const int32_t* 
     p.nslices = (V + p.slice - 1) / p.slice;
     p.dslice = draw_slice(B, V, dtype);
     p.ndslices = (V + p.dslice - 1) / p.dslice;
+    p.sms = device_sms();
     // the resolving CTA gathers the chunk masses of a whole drawn row in shared memory
     if (p.ndslices * (p.dslice / (4 * 32 * (dtype == SPEC_F32 ? 4 : 8))) > specv::kMaxRowChunks) return SPEC_ERR_ARG;
     p.vec = vec ? 1 : 0;

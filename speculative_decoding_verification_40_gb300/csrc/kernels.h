@@ -55,6 +55,8 @@ struct SampleParams {
   int ndslices;              // draw CTAs per batch row (<= kMaxSlices)
   int vec;                   // every logit row starts on a 16-byte boundary
   int step;                  // 0: stream every position; i + 1: stream position i of the rows still verifying
+  int cluster;               // draw kernel: the ndslices CTAs of a row form one thread-block cluster
+  int sms;                   // streaming multiprocessors of the device (host side; 0 if unknown)
   int32_t* emitted;          // [B, G+1]
   int32_t* n_acc;            // [B]
   Workspace ws;
