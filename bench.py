@@ -6,11 +6,12 @@ A step is one spec_verify_sample call (accept test, first rejection, residual
 / bonus inverse-CDF draw; every row of the hot path) over one batch of the
 seeded synthetic workload, inputs resident in HBM.  The default workload is c3
 (B=256, gamma=5, V=152064, fp32 logits, T=0.7): 1.71 GB of logits per call,
-13x the L2, so no flush is needed between calls.  Prints one JSON line.
+13x the L2; three copies of the logits are used in turn, so no call reads
+logits an earlier call left in L2.  Prints one JSON line.
 
---impl reference times the float64 CPU oracle (the reference implementation
-of the method for this build) on the same workload and metric, over a bounded
-sample of rows per step.  Under torchrun each rank runs its own replica of the
+--impl reference times the float64 CPU oracle (the only reference
+implementation of the method: the pages it follows publish no code) on the
+same workload and metric, over a bounded sample of rows per step.  Under torchrun each rank runs its own replica of the
 workload on its own GPU (no data-path collective); rank 0 prints.
 """
 from __future__ import annotations
