@@ -628,7 +628,11 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_stream_kernel(const 
   __shared__ float rawr[kSW];
   __shared__ int last;
   const int tid = threadIdx.x;
-  // the draw kernel may be scheduled once every stream CTA is running; it waits for their results
+  // Launched as a programmatic dependent of whatever precedes it on the stream (the previous call's
+  // draw kernel, the previous early-exit position, or the caller's kernel that wrote the logits): its
+  // CTAs may be resident early, and read nothing until that grid has finished and its writes are
+  // visible.  Only then may the draw kernel be scheduled (it reads the row inputs before its own wait).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
   const int NS = a.nslices;
   const int s = blockIdx.x % NS;
@@ -645,11 +649,7 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_stream_kernel(const 
   const int pos = b * G1 + i;
   const int gb = a.draft_len ? __ldg(a.draft_len + b) : a.G;
   if (gb < 0 || gb > a.G || i > gb) return;  // invalid length (the draw kernel reports it) or padding
-  if (a.step) {
-    // launched as a programmatic dependent of the previous position's launch: wait for its decisions
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (__ldcg(a.ws.stop + b) != 0) return;
-  }
+  if (a.step && __ldcg(a.ws.stop + b) != 0) return;  // the previous positions' decisions (waited for above)
   const bool has_q = i < gb;
   const float sc = a.scale;
   const int lo = s * a.slice;
@@ -841,6 +841,8 @@ template <typename T>
 __global__ void __launch_bounds__(kStreamThreads, 4) verify_draw_kernel(const SampleParams a) {
   __shared__ DrawSmem sm;
   if (a.cluster) cluster_arrive_relaxed();  // this CTA has started (its shared memory may be written)
+  // the next call's stream kernel may be scheduled now; it waits for this grid before reading anything
+  asm volatile("griddepcontrol.launch_dependents;");
   const int ND = a.ndslices;
   const int b = a.B - 1 - static_cast<int>(blockIdx.x / ND);  // last-streamed rows first: still in L2
   const int d = static_cast<int>(blockIdx.x % ND);
@@ -863,6 +865,9 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_draw_kernel(const Sa
 // remove the second launch and the round trip between the two kernels.
 template <typename T, bool kMask>
 __global__ void __launch_bounds__(kStreamThreads, 4) verify_short_kernel(const SampleParams a) {
+  // a programmatic dependent of the previous launch on the stream: read nothing before it has finished
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
   __shared__ DrawSmem sm;
   constexpr int kV = Elems<T>::kVec;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -944,6 +949,14 @@ static bool short_rows(const SampleParams& p, size_t esz) {
          p.nslices == 1 && p.ndslices == 1;
 }
 
+// The first kernel of a sampling call is launched as a programmatic dependent of the launch before it on
+// the stream (its CTAs wait in griddepcontrol.wait before reading anything), so back-to-back calls do
+// not pay a launch gap.  SPECVERIFY_PDL=0 launches it plainly.
+static bool pdl_first() {
+  const char* env = std::getenv("SPECVERIFY_PDL");
+  return !(env && std::atoi(env) == 0);
+}
+
 // A row's draw CTAs form one cluster when there are 2 to 8 of them (the portable cluster size) and the
 // whole draw grid is at most one CTA per SM: their chunk masses meet in rank 0's shared memory at a
 // cluster barrier instead of going through the workspace behind an arrival counter, which shortens the
@@ -988,7 +1001,7 @@ cudaError_t sample_early_exit_launch(SampleParams p, int dtype, cudaStream_t str
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = i > 0 ? 1 : 0;  // each position's launch overlaps the previous one's tail
+    cfg.numAttrs = (i > 0 || pdl_first()) ? 1 : 0;  // each position's launch overlaps the previous one's tail
     const cudaError_t e = dtype == 0 ? cudaLaunchKernelEx(&cfg, verify_stream_kernel<float, false>, p)
                                      : cudaLaunchKernelEx(&cfg, verify_stream_kernel<__nv_bfloat16, false>, p);
     if (e != cudaSuccess) return e;
@@ -1358,17 +1371,27 @@ cudaError_t rows_sample_launch(const SampleParams& p, int dtype, cudaStream_t st
               : rows_sample_launch_t<__nv_bfloat16, false>(p, stream);
 }
 
+template <typename K>
+static cudaError_t launch_first(K kernel, dim3 grid, const SampleParams& p, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kStreamThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_first() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 template <typename T, bool kMask>
 static cudaError_t sample_launch_t(const SampleParams& p, int phases, cudaStream_t stream) {
-  const dim3 block(kStreamThreads);
-  if (phases == 3 && short_rows(p, sizeof(T))) {
-    verify_short_kernel<T, kMask><<<dim3(static_cast<unsigned>(p.B)), block, 0, stream>>>(p);
-    return cudaGetLastError();
-  }
+  if (phases == 3 && short_rows(p, sizeof(T)))
+    return launch_first(verify_short_kernel<T, kMask>, dim3(static_cast<unsigned>(p.B)), p, stream);
   const dim3 g1(static_cast<unsigned>((long long)p.B * (p.G + 1) * p.nslices));
   if (phases & 1) {
-    verify_stream_kernel<T, kMask><<<g1, block, 0, stream>>>(p);
-    const cudaError_t e = cudaGetLastError();
+    const cudaError_t e = launch_first(verify_stream_kernel<T, kMask>, g1, p, stream);
     if (e != cudaSuccess) return e;
   }
   return (phases & 2) ? launch_draw<T>(p, stream) : cudaSuccess;
