@@ -26,6 +26,23 @@
  *    [0, 1), draft_len outside [0, gamma]) marks the affected batch row
  *    invalid -- n_accepted[b] = -1 and emitted[b, :] = -1 -- and is recorded in
  *    the workspace's error word, read by spec_check_status.
+ *  - The first kernel of a sampling call is launched as a programmatic
+ *    dependent of the launch before it on `stream` (CUDA programmatic dependent
+ *    launch): its thread blocks may become resident while that kernel drains,
+ *    but they read no input and write no output or workspace slot before it
+ *    has finished and its writes are visible, so stream order holds as for a
+ *    plain launch.  The last kernel of a call allows the next launch on the
+ *    stream to be scheduled early; a caller's kernel launched that way must
+ *    itself wait (griddepcontrol.wait / cudaGridDependencySynchronize) before
+ *    it reads this call's outputs, as programmatic launches require.
+ *  - Tuning overrides read from the environment at every call (for
+ *    measurements; results are the same up to float32 rounding order within
+ *    the documented tolerances): SPECVERIFY_SLICE / SPECVERIFY_DSLICE (stream /
+ *    draw slice, elements), SPECVERIFY_EE_SLICE (early-exit slice),
+ *    SPECVERIFY_CLUSTER / SPECVERIFY_STATS_SLICE (statistics cluster size /
+ *    slice), SPECVERIFY_DRAW_CLUSTER (0 / 1: a row's draw CTAs as a
+ *    thread-block cluster), SPECVERIFY_PDL=0 (plain launch of a call's first
+ *    kernel).
  *  - A row is invalid if any logit row it reads holds a NaN or +inf or is
  *    entirely -inf.  Ragged rows (draft_len[b] = gamma_b < gamma) never read
  *    target rows i > gamma_b, draft rows i >= gamma_b, ids i >= gamma_b, or
