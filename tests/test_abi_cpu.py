@@ -112,6 +112,20 @@ def test_launch_plans_for_the_five_workloads(B, G, V, bf16, cs, monkeypatch):
     assert p["smem_bytes"] <= 227 * 1024
 
 
+@pytest.mark.parametrize("B,G,V,ctas", [
+    (8, 4, 32128, 8),       # c1: 40 positions x 4 slices of 8192 < 2 x 152 SMs -> slices of 4096
+    (1, 4, 1024, 1),        # c0: one slice whatever its size
+    (2, 1, 16384, 8),       # 4 positions: halved down to the 2048-element floor
+    (64, 8, 128256, 16),    # c2: 576 positions fill the GPU at 8192
+    (256, 5, 152064, 19),   # c3
+])
+def test_greedy_slices_fill_the_gpu_for_small_batches(B, G, V, ctas):
+    # without a device the rule assumes 152 SMs: slices of 8192 target elements, halved (to 2048 at
+    # least) while the batch gives fewer than two CTAs per SM
+    import torch
+    assert S.plan(B, G, V, torch.bfloat16)["greedy_ctas_per_row"] == ctas
+
+
 def test_sample_rows_rejects_bad_arguments_on_the_host():
     L = S.lib
     p = ctypes.c_void_p(4096)
