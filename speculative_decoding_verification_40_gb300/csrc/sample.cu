@@ -958,16 +958,16 @@ static bool pdl_first() {
 }
 
 // A row's draw CTAs form one cluster when there are 2 to 8 of them (the portable cluster size) and the
-// whole draw grid is at most one CTA per SM: their chunk masses meet in rank 0's shared memory at a
-// cluster barrier instead of going through the workspace behind an arrival counter, which shortens the
-// latency-bound draw of a small batch (c1: 16.7 vs 18.8 us per call).  A larger draw grid keeps the
-// counter: its CTAs take SM slots one by one as the stream kernel drains, where a cluster waits for
-// ndslices free slots in one GPC (c2: 65.2 vs 64.5 us per call with clusters).
+// whole draw grid is resident at once (at most 4 CTAs per SM): their chunk masses meet in rank 0's
+// shared memory at a cluster barrier instead of going through the workspace behind an arrival counter,
+// which shortens the draw's chain of round trips (c1: 16.7 vs 18.8 us per call; c2, back to back: 60.3
+// vs 62.1 us).  A draw grid of more than one wave keeps the counter: its CTAs take SM slots one by one
+// as the stream kernel drains, where a cluster waits for ndslices free slots in one GPC.
 // SPECVERIFY_DRAW_CLUSTER=0 / 1 forces the counter / the cluster for 2 to 8 draw CTAs per row.
 static bool draw_clusters(const SampleParams& p) {
   if (p.ndslices < 2 || p.ndslices > 8) return false;
   if (const char* env = std::getenv("SPECVERIFY_DRAW_CLUSTER")) return std::atoi(env) != 0;
-  return static_cast<long long>(p.B) * p.ndslices <= (p.sms > 0 ? p.sms : 152);
+  return static_cast<long long>(p.B) * p.ndslices <= 4LL * (p.sms > 0 ? p.sms : 152);
 }
 
 template <typename T>
