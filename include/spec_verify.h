@@ -72,7 +72,7 @@ typedef enum {
   SPEC_ERR_CUDA = 3,         /* a CUDA runtime call failed */
   SPEC_ERR_NONFINITE = 4,    /* a logit row read holds NaN / +inf or is all -inf */
   SPEC_ERR_TOKEN_RANGE = 5,  /* a draft id read lies outside [0, V) */
-  SPEC_ERR_TIMEOUT = 6,      /* reserved: no entry point waits on another block */
+  SPEC_ERR_TIMEOUT = 6,      /* reserved: no entry point polls for another block's progress */
   SPEC_ERR_WORKSPACE = 7,    /* workspace too small or not 256-byte aligned */
   SPEC_ERR_BOUNDS = 8        /* an index check failed: only libspecverify_debug.so (built with
                                 -DSPEC_DEBUG_BOUNDS) checks kernel indices and reports this */
