@@ -171,15 +171,21 @@ int spec_verify_sample_early_exit(const void* target_logits, const void* draft_l
  * library, held by every GPU that loads the library until the process exits.
  * Calls whose spec_workspace_size(B, gamma, V, dtype) exceeds it return
  * SPEC_ERR_WORKSPACE without touching the GPU (use spec_verify_sample with a
- * workspace of your own then).  The first call on a device looks up the
- * array's device address on that device (cudaGetSymbolAddress); make that first
- * call before any stream capture.  Every call uses the same array, so calls
- * that overlap on the GPU (other streams, other threads) race and corrupt each
+ * workspace of your own then); so does every other argument error
+ * spec_verify_sample reports on the host (SPEC_ERR_ARG, SPEC_ERR_DTYPE): the
+ * array is left as it was.  The first call on a device looks up the array's
+ * device address on that device (cudaGetSymbolAddress) and keeps it; make that
+ * first call before any stream capture, and do not call this entry point on a
+ * device after cudaDeviceReset of that device in the same process (the kept
+ * address would be stale).  Every call uses the same array, so calls that
+ * overlap on the GPU (other streams, other threads) race and corrupt each
  * other's results: serialise them.  Each call clears the counters it needs at
  * zero on `stream` before its kernels (cudaMemsetAsync; nothing is allocated).
- * Device-side findings are reported through n_accepted[b] = -1 and
- * emitted[b, :] = -1 only, since the caller has no workspace to read an error
- * word from.  Arguments, layouts and results otherwise as spec_verify_sample. */
+ * The input checks the device makes (non-finite or all -inf logit rows, draft
+ * ids outside [0, V), uniforms outside [0, 1), draft_len outside [0, gamma])
+ * show as n_accepted[b] = -1 and emitted[b, :] = -1 only, since the caller has
+ * no workspace to read an error word from.  Arguments, layouts and results
+ * otherwise as spec_verify_sample. */
 #define SPEC_NOALLOC_SCRATCH_BYTES (16u << 20)
 int spec_verify_sample_noalloc(const void* target_logits, const void* draft_logits, int dtype,
                                const int32_t* draft_ids, const int32_t* draft_len, const float* uniforms,

@@ -54,6 +54,9 @@ the design notes):
       The pages state the scaling of q in the comparison and the resulting
       guarantee (no token drawn with probability above p(x)/l), not the
       residual; this residual is the plainest reading and meets the guarantee.
+      PARITY UNPINNED for the lenient residual (verify_row with lenience < 1):
+      the pages fix the bound and the acceptance rate sum min(q, p/l), which
+      are pinned, but nothing they print fixes the residual itself.
   R10 nucleus (top-p) keeps every token whose logit is >= that of the token at
       which the descending running probability first reaches top_p (ties kept);
       top_p >= 1 keeps everything.  A standardised row is the logit row with
@@ -158,6 +161,23 @@ def inverse_cdf(w: np.ndarray, u: float):
     return k, bool(flagged)
 
 
+def draw_boundary_probability(w: np.ndarray) -> float:
+    """Probability, over a final uniform u ~ U[0, 1), that R8 flags the draw from weights w.
+
+    The draw lands in cell k (normalised width c_k = w_k / Z) and is flagged when u lies within 1e-5 of
+    one of that cell's two edges; both strips lie inside the cell, so cell k contributes min(c_k, 2e-5).
+    """
+    Z = float(np.sum(w))
+    c = np.asarray(w, dtype=np.float64)[np.asarray(w) > 0] / Z
+    return float(np.minimum(c, 2.0 * BOUNDARY_EPS).sum())
+
+
+def accept_boundary_probability(r: float) -> float:
+    """Probability, over u ~ U[0, 1), that an accept test with threshold r is flagged by R8: the length of
+    [0, 1) within 1e-5 of r."""
+    return max(0.0, min(1.0, r + BOUNDARY_EPS) - max(0.0, r - BOUNDARY_EPS))
+
+
 def draw_candidates(w: np.ndarray, u: float) -> list[int]:
     """Tokens whose normalised CDF cell [C_{k-1}/Z, C_k/Z] (w_k > 0) lies within 1e-5 of u (R8).
 
@@ -182,7 +202,7 @@ def verify_row(tl: np.ndarray, dl: np.ndarray, ids: np.ndarray, gb: int, u: np.n
     gamma = dl.shape[0]
     V = tl.shape[1]
     bad = dict(emitted=[-1] * (gamma + 1), n=-1, boundary=False, valid=False, accept_boundary=False,
-               candidates=[])
+               candidates=[], flag_prob=0.0)
     if not (0 <= gb <= gamma):
         return bad
     for i in range(gb + 1):
@@ -204,11 +224,13 @@ def verify_row(tl: np.ndarray, dl: np.ndarray, ids: np.ndarray, gb: int, u: np.n
     # Phase 3: walk the guesses left to right, stop at the first rejection.
     n = gb
     boundary = False
+    flag_prob = 0.0       # expected R8 flags of this row had its tested uniforms been fresh draws
     for i in range(gb):
         x = int(ids[i])
         px, qx = p[i][x], q[i][x]
         lq = lenience * qx                         # R11: lenience scales q [p1 §5, Appendix A.5]
         r = 1.0 if px >= lq else px / lq          # min(1, p/q) [p1 §2.3 Phase 3]
+        flag_prob += accept_boundary_probability(r)
         if abs(u[i] - r) < BOUNDARY_EPS:
             boundary = True
         if not (px > 0.0 and u[i] <= r):          # R3
@@ -223,12 +245,13 @@ def verify_row(tl: np.ndarray, dl: np.ndarray, ids: np.ndarray, gb: int, u: np.n
     else:
         w = p[gb]                                  # bonus t ~ p_{gamma+1} [p1 Phase 4]
     tok, flag = inverse_cdf(w, float(u[gamma]))
+    flag_prob += draw_boundary_probability(w)
     accept_boundary = boundary
     boundary = boundary or flag
     emitted = [int(ids[i]) for i in range(n)] + [tok] + [-1] * (gamma - n)
     cands = draw_candidates(w, float(u[gamma])) if flag else [tok]
     return dict(emitted=emitted, n=n, boundary=boundary, valid=True, accept_boundary=accept_boundary,
-                candidates=cands)
+                candidates=cands, flag_prob=flag_prob)
 
 
 def greedy_row(tl: np.ndarray, ids: np.ndarray, gb: int, gamma: int):
@@ -291,7 +314,10 @@ def verify_sample(target, draft, dtype, ids, draft_len, uniforms, T, rows=None, 
 
     `rows` restricts the work to a subset of b (the outputs still have B rows;
     rows not computed hold -2).  Returns dict of numpy arrays: emitted
-    [B,gamma+1] int64, n_accepted [B], boundary [B] bool, valid [B] bool.
+    [B,gamma+1] int64, n_accepted [B], boundary [B] bool, valid [B] bool, and
+    flag_prob [B], the probability that R8 would flag the row if each tested
+    uniform and the final one were fresh U[0, 1) draws (the expected boundary
+    count of a batch is its sum).
     """
     B, G1, V = target.shape
     gamma = G1 - 1
@@ -303,6 +329,7 @@ def verify_sample(target, draft, dtype, ids, draft_len, uniforms, T, rows=None, 
     boundary = np.zeros(B, dtype=bool)
     accept_boundary = np.zeros(B, dtype=bool)
     valid = np.zeros(B, dtype=bool)
+    flag_prob = np.zeros(B)
     candidates = {}
     for b in (range(B) if rows is None else rows):
         gb = int(gl[b])
@@ -318,9 +345,10 @@ def verify_sample(target, draft, dtype, ids, draft_len, uniforms, T, rows=None, 
         boundary[b] = res["boundary"]
         accept_boundary[b] = res["accept_boundary"]
         valid[b] = res["valid"]
+        flag_prob[b] = res["flag_prob"]
         candidates[b] = res["candidates"]
     return dict(emitted=emitted, n_accepted=n_acc, boundary=boundary, accept_boundary=accept_boundary,
-                valid=valid, candidates=candidates)
+                valid=valid, candidates=candidates, flag_prob=flag_prob)
 
 
 def sample_rows(logits, dtype, uniforms, T, rows=None, thr=None):

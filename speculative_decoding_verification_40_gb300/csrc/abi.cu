@@ -246,6 +246,27 @@ int check_sizes(int dtype, int B, int gamma, int V) {
   return SPEC_OK;
 }
 
+}  // namespace
+
+namespace specv {
+
+// Host-side checks of the sampling entry points' arguments other than the workspace: sizes, dtype,
+// temperature and the pointers a call with B > 0 dereferences.
+int check_sample_args(const void* target, const void* draft, int dtype, const int32_t* ids, const float* uniforms,
+                      float temperature, int B, int gamma, int V, const int32_t* emitted, const int32_t* n_accepted) {
+  const int st = check_sizes(dtype, B, gamma, V);
+  if (st != SPEC_OK) return st;
+  if (!(std::isfinite(temperature) && temperature > 0.f)) return SPEC_ERR_ARG;
+  if (B == 0) return SPEC_OK;
+  if (target == nullptr || uniforms == nullptr || emitted == nullptr || n_accepted == nullptr) return SPEC_ERR_ARG;
+  if (gamma > 0 && (draft == nullptr || ids == nullptr)) return SPEC_ERR_ARG;
+  return SPEC_OK;
+}
+
+}  // namespace specv
+
+namespace {
+
 int check_common(int dtype, int B, int gamma, int V, const void* workspace, size_t ws_bytes) {
   const int st = check_sizes(dtype, B, gamma, V);
   if (st != SPEC_OK || B == 0) return st;

@@ -62,6 +62,11 @@ struct SampleParams {
   Workspace ws;
 };
 
+// Host-side argument checks of the sampling entry points other than the workspace (sizes, dtype,
+// temperature, pointers); a spec_status_t.
+int check_sample_args(const void* target, const void* draft, int dtype, const int32_t* ids, const float* uniforms,
+                      float temperature, int B, int gamma, int V, const int32_t* emitted, const int32_t* n_accepted);
+
 // dtype: 0 = float32, 1 = bfloat16.  stats selects the statistics kernel.
 cudaError_t stats_prepare(int dtype);
 cudaError_t stats_max_active_clusters(int dtype, int cs, int* out);

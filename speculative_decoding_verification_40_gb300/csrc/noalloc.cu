@@ -5,6 +5,7 @@
 
 #include "../../include/spec_verify.h"
 #include "common.cuh"
+#include "kernels.h"
 
 namespace {
 
@@ -14,7 +15,9 @@ constexpr int kMaxDevices = 64;
 // Zero-initialised at module load on every device that loads the library, and kept until exit.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocBytes];
 
-// Device address of g_noalloc_scratch on each device; the host-side symbol is only a stand-in.
+// Device address of g_noalloc_scratch on each device; the host-side symbol is only a stand-in.  Resolved
+// once per device by the first call there; a cudaDeviceReset of that device invalidates it (the array's
+// new address is not looked up again).
 void* g_scratch_addr[kMaxDevices];
 std::mutex g_scratch_mu;
 
@@ -47,8 +50,12 @@ extern "C" int spec_verify_sample_noalloc(const void* target_logits, const void*
   if (need == 0) return (dtype != SPEC_F32 && dtype != SPEC_BF16) ? SPEC_ERR_DTYPE : SPEC_ERR_ARG;
   if (need > kNoallocBytes) return SPEC_ERR_WORKSPACE;  // beyond the fixed scratch: use spec_verify_sample
   if (B == 0) return SPEC_OK;
+  // every argument check before the shared array is touched: a rejected call leaves it as it was
+  int st = specv::check_sample_args(target_logits, draft_logits, dtype, draft_ids, uniforms, temperature, B, gamma,
+                                    V, emitted, n_accepted);
+  if (st != SPEC_OK) return st;
   void* scratch = nullptr;
-  int st = scratch_address(&scratch);
+  st = scratch_address(&scratch);
   if (st != SPEC_OK) return st;
   // The error word and the per-row arrival counters must start at zero; every other slot is either
   // written before it is read or left at zero by the previous call.

@@ -18,8 +18,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def test_reference_arm_prints_one_contract_line():
-    cmd = [sys.executable, "bench.py", "--impl", "reference", "--workload", "c1", "--steps", "2", "--warmup", "1",
-           "--ref-rows", "2"]
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--workload", "c1", "--steps", "2", "--warmup", "1"]
     r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
@@ -30,7 +29,10 @@ def test_reference_arm_prints_one_contract_line():
         assert key in d, key
     assert d["impl"] == "reference" and d["warmup"] >= 3 and d["value"] > 0 and d["higher_is_better"] is True
     assert d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
-    assert d["config"]["workload"].startswith("c1")
+    assert d["config"]["workload"].startswith("c1") and d["config"]["B"] == 8
+    # whole batches: the claimed time is the timed steps' own wall time
+    assert d["steps"] == 2 and d["ms_per_step"] > 0
+    assert abs(d["value"] - d["config"]["positions_per_step"] / (d["ms_per_step"] * 1e-3)) < 1e-6 * d["value"]
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
 

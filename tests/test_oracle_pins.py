@@ -343,6 +343,46 @@ def test_draw_candidates_cover_the_near_edge_tokens():
     assert O.draw_candidates(w, 0.25) == [0]
 
 
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_boundary_probability_is_the_flagged_fraction_of_uniforms(seed):
+    """R8's expected flag rate, checked by brute force: over a fine stratified grid of final uniforms, the
+    fraction that inverse_cdf flags equals draw_boundary_probability (cells wider and narrower than the
+    2e-5 band, zero weights, a dominant token), and over accept uniforms the fraction within 1e-5 of r
+    equals accept_boundary_probability (r inside, at 1, near 0)."""
+    rng = np.random.default_rng(seed)
+    w = np.concatenate([rng.random(6), rng.random(40) * 1e-6, [0.0, 0.0], [3.0]])
+    rng.shuffle(w)
+    N = 400_000
+    u = (np.arange(N) + 0.5) / N
+    Z = w.sum()
+    C = np.cumsum(w)
+    k = np.searchsorted(C, u * Z, side="right")
+    lo = np.where(k > 0, C[np.maximum(k - 1, 0)], 0.0)
+    hi = C[np.minimum(k, w.size - 1)]
+    flagged = (np.abs(u * Z - lo) / Z < O.BOUNDARY_EPS) | (np.abs(u * Z - hi) / Z < O.BOUNDARY_EPS)
+    # the vectorised test above is inverse_cdf's own flag; spot-check that on a few uniforms
+    for j in range(0, N, N // 50):
+        assert O.inverse_cdf(w, float(u[j]))[1] == bool(flagged[j])
+    assert flagged.mean() == pytest.approx(O.draw_boundary_probability(w), abs=3.0 / N)
+    for r in (0.5, 1.0, 3e-6, 0.0, 0.99999):
+        frac = (np.abs(u - r) < O.BOUNDARY_EPS).mean()
+        assert frac == pytest.approx(O.accept_boundary_probability(r), abs=3.0 / N)
+
+
+def test_boundary_probability_of_a_row_sums_its_tested_positions():
+    """verify_row's flag_prob: one accept band per tested position (up to and including the first
+    rejection) plus the final draw's band mass."""
+    p = np.array([[0.3, 0.7], [0.5, 0.5]])
+    q = np.array([[0.6, 0.4]])
+    tl, dl = np.log(p), np.log(q)
+    rej = O.verify_row(tl, dl, np.array([0]), 1, np.array([0.9, 0.3]), 1.0)     # rejected: residual (0, 1)
+    assert rej["n"] == 0
+    assert rej["flag_prob"] == pytest.approx(2e-5 + min(1.0, 2e-5))
+    acc = O.verify_row(tl, dl, np.array([0]), 1, np.array([0.1, 0.3]), 1.0)     # accepted: bonus (0.5, 0.5)
+    assert acc["n"] == 1
+    assert acc["flag_prob"] == pytest.approx(2e-5 + 4e-5)
+
+
 # ----------------------------------------------------------------------------- draft-side sampler
 
 def _stratified(N):
@@ -511,13 +551,25 @@ def test_lenience_keeps_the_pages_bound(case, l):
     if gamma >= 1:
         accept = sum(v for k, v in law.items() if len(k) >= 2)
         assert accept == pytest.approx(np.minimum(q[0], p[0] / l).sum(), abs=1e-12)
-        # R11's first-token law: accepted mass min(q, p/l), then the rejection mass spread over the
-        # residual max(0, p - l q) normalised
-        acc = np.minimum(q[0], p[0] / l)
-        resid = np.maximum(0.0, p[0] - l * q[0])
-        R = 1.0 - acc.sum()
-        expect = acc + (R * resid / resid.sum() if resid.sum() > 0 else 0.0)
-        assert np.max(np.abs(first - expect)) < 1e-12
+
+
+@pytest.mark.parametrize("l", [0.1, 0.5, 0.9])
+@pytest.mark.parametrize("case", list(all_small_cases(seed=13))[::2], ids=lambda c: f"V{c[0]}g{c[1]}")
+def test_lenient_residual_consistency_not_a_pin(case, l):
+    """Consistency check, not a pin: the pages state the scaled comparison and the p(x)/l bound but
+    not the residual drawn after a lenient rejection, so R11's norm(max(0, p - l q)) rests on a
+    reading.  This only checks that the oracle's measured first-token law is the one that reading
+    implies (accepted mass min(q, p/l), the rejection mass spread over the normalised residual);
+    it restates the reading's formula and cannot show the reading itself is the pages'."""
+    V, gamma, p, q = case
+    if gamma < 1:
+        return
+    first = first_token_marginal(measure_law(_lenient_run(l), p, q), V)
+    acc = np.minimum(q[0], p[0] / l)
+    resid = np.maximum(0.0, p[0] - l * q[0])
+    R = 1.0 - acc.sum()
+    expect = acc + (R * resid / resid.sum() if resid.sum() > 0 else 0.0)
+    assert np.max(np.abs(first - expect)) < 1e-12
 
 
 def test_lenience_one_is_the_exact_method():

@@ -66,6 +66,14 @@ class Workload:
     row_kind: torch.Tensor | None = None    # [B] int8 (ROW_* codes)
     meta: dict = field(default_factory=dict)
 
+    def to(self, device) -> "Workload":
+        """The same workload with every tensor copied to `device` (one copy per tensor)."""
+        mv = lambda t: None if t is None else t.to(device)  # noqa: E731
+        return Workload(name=self.name, B=self.B, gamma=self.gamma, V=self.V, dtype=self.dtype, T=self.T,
+                        target=mv(self.target), draft=mv(self.draft), ids=mv(self.ids), uniforms=mv(self.uniforms),
+                        draft_len=mv(self.draft_len), greedy_ids=mv(self.greedy_ids), row_kind=mv(self.row_kind),
+                        meta=self.meta)
+
     def positions(self) -> int:
         """Verified draft positions in one call: sum over rows of gamma_b."""
         if self.draft_len is None:
