@@ -38,7 +38,8 @@
  *  - Tuning overrides read from the environment at every call (for
  *    measurements; results are the same up to float32 rounding order within
  *    the documented tolerances): SPECVERIFY_SLICE / SPECVERIFY_DSLICE (stream /
- *    draw slice, elements), SPECVERIFY_EE_SLICE (early-exit slice),
+ *    draw slice, elements), SPECVERIFY_ROW_CLUSTER (CTAs per batch row of the
+ *    early exit's one-launch kernel), SPECVERIFY_EARLY_FORM (see the early exit),
  *    SPECVERIFY_CLUSTER / SPECVERIFY_STATS_SLICE (statistics cluster size /
  *    slice), SPECVERIFY_DRAW_CLUSTER (0 / 1: a row's draw CTAs as a
  *    thread-block cluster), SPECVERIFY_PDL=0 (plain launch of a call's first
@@ -72,7 +73,7 @@ typedef enum {
   SPEC_ERR_CUDA = 3,         /* a CUDA runtime call failed */
   SPEC_ERR_NONFINITE = 4,    /* a logit row read holds NaN / +inf or is all -inf */
   SPEC_ERR_TOKEN_RANGE = 5,  /* a draft id read lies outside [0, V) */
-  SPEC_ERR_TIMEOUT = 6,      /* reserved: no entry point polls for another block's progress */
+  SPEC_ERR_TIMEOUT = 6,      /* a bounded wait of the early exit's one-launch kernel ran out */
   SPEC_ERR_WORKSPACE = 7,    /* workspace too small or not 256-byte aligned */
   SPEC_ERR_BOUNDS = 8        /* an index check failed: only libspecverify_debug.so (built with
                                 -DSPEC_DEBUG_BOUNDS) checks kernel indices and reports this */
@@ -80,8 +81,8 @@ typedef enum {
 
 /* Bytes of device workspace the entry points need for (B, gamma, V): an error
  * word, per-row arrival counters, greedy argmax keys, per-slice softmax
- * normalisers, the logits at the draft tokens, the chunk masses of the drawn
- * rows, and the early exit's stop positions.  The workspace must be zero-filled once before its first
+ * normalisers, the logits at the draft tokens, and the chunk masses of the
+ * drawn rows.  The workspace must be zero-filled once before its first
  * use (cudaMemset or spec_workspace_init); every call leaves the slots it used
  * at zero again, so one workspace serves any sequence of calls of any shape on
  * one stream.  Calls that overlap on the GPU must use different workspaces.
@@ -141,18 +142,28 @@ int spec_verify_sample_draw(const void* target_logits, const void* draft_logits,
                             int32_t* emitted, int32_t* n_accepted,
                             void* workspace, size_t ws_bytes, void* stream);
 
-/* Byte-lean early exit: spec_verify_sample that reads position i + 1 of a batch
- * row only while the row has not stopped.  Positions are verified one after
- * the other (one streaming launch per position, gamma + 1 in all, then the
- * draw launch); after each, the row stops at its first rejection, at an
- * invalid position, or at the bonus position gamma_b.  The logits read per row
- * are then the n + 1 target and n + 1 draft rows up to the first rejection n
- * (n + 1 target and n draft rows for a bonus draw) instead of 2 gamma_b + 1:
- * about sum_k alpha^k rows when each guess is accepted with probability alpha
- * (§3.1).  For valid inputs the outputs are exactly spec_verify_sample's (the
- * same arithmetic decides every position and draws).  A logit row after the
- * first rejection is never read, so a NaN / +inf or all -inf row there does
- * not make the batch row invalid as it does in spec_verify_sample.  Arguments,
+/* Byte-lean early exit: spec_verify_sample that takes position i + 1 of a batch
+ * row into account only while the row has not stopped -- at its first
+ * rejection, at an invalid position, or at the bonus position gamma_b.  A
+ * logit row after the first rejection does not count, so a NaN / +inf or all
+ * -inf row there does not make the batch row invalid as it does in
+ * spec_verify_sample; ids and uniforms of every position are still checked.
+ * Two forms, chosen per call by the batch's size:
+ *  - one launch of a kernel with a thread-block cluster per batch row, which
+ *    decides each position before streaming the next, so a row reads the n + 1
+ *    target and n + 1 draft rows up to its first rejection n (n + 1 and n for a
+ *    bonus draw) instead of 2 gamma_b + 1: about sum_k alpha^k rows when each
+ *    guess is accepted with probability alpha (§3.1).  Taken when one position
+ *    of the batch (2 B V logits) is at least 64 MB; it splits the vocabulary its
+ *    own way, so its float32 sums round differently from spec_verify_sample's
+ *    and a draw within about 1e-6 of a CDF edge may pick the neighbouring token;
+ *  - otherwise spec_verify_sample's two kernels, with the decisions taken as
+ *    above: exactly spec_verify_sample's outputs for valid inputs (smaller
+ *    batches gain nothing from skipping rows: their per-position latency
+ *    outweighs the bytes).
+ * SPECVERIFY_EARLY_FORM=1 / 2 forces the one-launch / two-kernel form.  A
+ * cluster slot that does not fill within about 0.1 s (which valid launches
+ * never see) marks the row invalid with SPEC_ERR_TIMEOUT.  Arguments,
  * layouts, workspace and the other errors as spec_verify_sample. */
 int spec_verify_sample_early_exit(const void* target_logits, const void* draft_logits, int dtype,
                                   const int32_t* draft_ids, const int32_t* draft_len, const float* uniforms,

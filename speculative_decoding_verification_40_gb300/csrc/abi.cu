@@ -102,6 +102,70 @@ int sample_slice(int V, int dtype, long long positions = 0) {
   return slice;
 }
 
+// Clusters of `cs` CTAs of the one-launch sampling kernel the current device holds at once (cached per
+// device, dtype and size); 0 if it cannot schedule one, -1 if the query fails.
+int rows_clusters(int dtype, int G, int cs) {
+  struct Entry {
+    int dev, dtype, G, cs, n;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (const Entry& e : cache)
+      if (e.dev == dev && e.dtype == dtype && e.G == G && e.cs == cs) return e.n;
+  }
+  int n = 0;
+  if (specv::rows_max_active_clusters(dtype, G, cs, &n) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  if (cache.size() < 1024) cache.push_back(Entry{dev, dtype, G, cs, n});
+  return n;
+}
+
+// Cluster size (CTAs per batch row) and slice length of the one-launch sampling kernel: slices of at
+// most 64 KB of a row, so CS = ceil(row bytes / 64 KB); a batch that would give fewer than four CTAs per
+// SM has its rows split further (CS doubled while slices stay at least 2 KB, at most 16 CTAs per row),
+// so that a small batch still spreads over the GPU (c2, B = 64 rows of 250 KB: 16 CTAs of 16 KB; c1,
+// B = 8: 16 CTAs of 4 KB).  A slice holds at most kMaxChunksPerSlice draw chunks, and the cluster size is
+// one the device can co-schedule (halved otherwise).  SPECVERIFY_ROW_CLUSTER (1 to 16) overrides.
+int rows_plan(int B, int G, int V, int dtype, int* cs_out, int* slice_out) {
+  const long long esz = dtype == SPEC_F32 ? 4 : 2;
+  const int kv = static_cast<int>(16 / esz);
+  const int cpc = 4 * 32 * kv;  // elements per draw chunk
+  const long long row = static_cast<long long>(V) * esz;
+  int cs = static_cast<int>((row + specv::kStreamSliceBytes - 1) / specv::kStreamSliceBytes);
+  if (cs < 1) cs = 1;
+  const long long want = 4LL * (device_sms() > 0 ? device_sms() : 152);
+  while (cs * 2 <= specv::kMaxCluster && static_cast<long long>(B) * cs < want && row / (cs * 2) >= 2048) cs *= 2;
+  if (const char* env = std::getenv("SPECVERIFY_ROW_CLUSTER")) {
+    const int w = std::atoi(env);
+    if (w >= 1 && w <= specv::kMaxCluster) cs = w;
+  }
+  if (cs > specv::kMaxCluster) cs = specv::kMaxCluster;
+  auto slice_of = [&](int c) { return static_cast<int>(align_up((V + c - 1) / c, kv)); };
+  while (cs < specv::kMaxCluster && (slice_of(cs) + cpc - 1) / cpc > specv::kMaxChunksPerSlice) ++cs;
+  for (;;) {
+    const int n = rows_clusters(dtype, G, cs);
+    if (n < 0) return SPEC_ERR_CUDA;
+    if (n > 0) break;
+    if (cs == 1) return SPEC_ERR_ARG;
+    cs /= 2;
+  }
+  const int L = slice_of(cs);
+  if ((L + cpc - 1) / cpc > specv::kMaxChunksPerSlice) return SPEC_ERR_ARG;
+  *cs_out = cs;
+  *slice_out = L;
+  return SPEC_OK;
+}
+
 // Falls back to smaller clusters when the device cannot co-schedule the planned one.
 int schedulable_plan(int V, int dtype, Plan* plan) {
   for (int tries = 0; tries < 5; ++tries) {
@@ -194,27 +258,6 @@ int draw_slice(int B, int V, int dtype) {
   if (const char* env = std::getenv("SPECVERIFY_DSLICE")) {
     const int want = std::atoi(env);
     if (want > 0) slice = want;
-  }
-  const int lo = (V + specv::kMaxSlices - 1) / specv::kMaxSlices;
-  if (slice < lo) slice = lo;
-  slice = static_cast<int>(align_up(slice, chunk));
-  if (slice > specv::kMaxChunksPerSlice * chunk) slice = specv::kMaxChunksPerSlice * chunk;
-  return slice;
-}
-
-// Early exit streams one position at a time, so a launch holds only the rows still verifying: slices
-// are cut so that the first position gives about four CTAs per SM (at most 32 slices per row, whole
-// draw chunks).  SPECVERIFY_EE_SLICE (elements) overrides within the same limits.
-int early_exit_slice(int B, int V, int dtype) {
-  const int chunk = 4 * 32 * (dtype == SPEC_F32 ? 4 : 8);
-  const long long want_ctas = 4LL * (device_sms() > 0 ? device_sms() : 152);
-  long long ns = (want_ctas + B - 1) / (B > 0 ? B : 1);
-  if (ns < 1) ns = 1;
-  if (ns > specv::kMaxSlices) ns = specv::kMaxSlices;
-  int slice = static_cast<int>((V + ns - 1) / ns);
-  if (const char* env = std::getenv("SPECVERIFY_EE_SLICE")) {
-    const int w = std::atoi(env);
-    if (w > 0) slice = w;
   }
   const int lo = (V + specv::kMaxSlices - 1) / specv::kMaxSlices;
   if (slice < lo) slice = lo;
@@ -324,11 +367,10 @@ int run_verify(const void* target, const void* draft, int dtype, const int32_t* 
     p.emitted = emitted;
     p.n_acc = n_accepted;
     p.ws = specv::ws_carve(workspace, B, gamma, V);
-    if (early_exit) {
-      p.slice = early_exit_slice(B, V, dtype);
-      p.nslices = (V + p.slice - 1) / p.slice;
-      return launch_status(specv::sample_early_exit_launch(p, dtype, static_cast<cudaStream_t>(stream)));
-    }
+    // the early exit's one-launch plan; without one (a cluster the device cannot schedule) the early exit
+    // takes the two-kernel path
+    if (early_exit && rows_plan(B, gamma, V, dtype, &p.rcs, &p.rslice) != SPEC_OK) p.rcs = 0;
+    if (early_exit) return launch_status(specv::sample_early_exit_launch(p, dtype, static_cast<cudaStream_t>(stream)));
     return launch_status(specv::sample_launch(p, dtype, phases, static_cast<cudaStream_t>(stream)));
   }
 

@@ -50,7 +50,6 @@ struct Workspace {
   float* part;               // [B, G+1, kMaxSlices] float4 slice normalisers (m_p, S_p, m_q, S_q)
   float* xl;                 // [B, G] float2 target / draft logit at the draft token
   float* dch;                // [B, chunks] float2 mass of each chunk of the drawn row(s)
-  int* stop;                 // [B] early exit: 0 while row b is verifying, n + 1 once it stopped at n
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -61,7 +60,7 @@ __host__ __device__ inline size_t chunks_per_row(int V) { return (size_t)(V + 12
 __host__ __device__ inline size_t ws_bytes_for(int B, int G, int V) {
   const size_t P = (size_t)B * (size_t)(G + 1);
   return 256 + align_up((size_t)B * 4, 256) + align_up(P * 8, 256) + align_up(P * kMaxSlices * 16, 256) +
-         align_up((size_t)B * G * 8, 256) + align_up((size_t)B * chunks_per_row(V) * 8, 256) + align_up((size_t)B * 4, 256);
+         align_up((size_t)B * G * 8, 256) + align_up((size_t)B * chunks_per_row(V) * 8, 256);
 }
 
 inline Workspace ws_carve(void* base, int B, int G, int V) {
@@ -79,8 +78,6 @@ inline Workspace ws_carve(void* base, int B, int G, int V) {
   w.xl = reinterpret_cast<float*>(p);
   p += align_up((size_t)B * G * 8, 256);
   w.dch = reinterpret_cast<float*>(p);
-  p += align_up((size_t)B * chunks_per_row(V) * 8, 256);
-  w.stop = reinterpret_cast<int*>(p);
   return w;
 }
 
@@ -110,9 +107,25 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
 }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
 
-// Store a float2 into shared memory of a CTA of this cluster (address from dsmem_map).
+// Split cluster barrier with ordering: shared-memory writes (local or distributed) before the arrive are
+// visible to every thread of the cluster after its matching wait.  Each thread alternates arrive / wait.
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Stores into shared memory of a CTA of this cluster (address from dsmem_map).
 __device__ __forceinline__ void dsmem_st_v2(uint32_t addr, float a, float b) {
   asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+}
+__device__ __forceinline__ void dsmem_st_v4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+__device__ __forceinline__ void dsmem_st_f32(uint32_t addr, float a) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(a) : "memory");
 }
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {

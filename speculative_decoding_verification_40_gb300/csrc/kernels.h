@@ -54,9 +54,11 @@ struct SampleParams {
   int dslice;                // vocabulary elements per draw CTA (a multiple of the draw chunk)
   int ndslices;              // draw CTAs per batch row (<= kMaxSlices)
   int vec;                   // every logit row starts on a 16-byte boundary
-  int step;                  // 0: stream every position; i + 1: stream position i of the rows still verifying
   int cluster;               // draw kernel: the ndslices CTAs of a row form one thread-block cluster
+  int rcs;                   // one-launch kernel: CTAs per batch row (thread-block cluster size, <= 16)
+  int rslice;                // one-launch kernel: vocabulary elements per CTA (a multiple of 16 bytes)
   int sms;                   // streaming multiprocessors of the device (host side; 0 if unknown)
+  int lazy;                  // draw kernel: early-exit validity (logit rows after the first rejection ignored)
   int32_t* emitted;          // [B, G+1]
   int32_t* n_acc;            // [B]
   Workspace ws;
@@ -71,10 +73,17 @@ int check_sample_args(const void* target, const void* draft, int dtype, const in
 cudaError_t stats_prepare(int dtype);
 cudaError_t stats_max_active_clusters(int dtype, int cs, int* out);
 cudaError_t stats_launch(const VerifyParams& p, int dtype, int cs, cudaStream_t stream);
-// phases: 1 = stream kernel, 2 = draw kernel, 3 = both
+// phases: 1 = stream kernel, 2 = draw kernel, 3 = both (or the short-row kernel for rows of at most 8 KB)
 cudaError_t sample_launch(const SampleParams& p, int dtype, int phases, cudaStream_t stream);
-// early exit: stream kernel once per position (p.step = i + 1, rows still verifying only), then the draw
+// early exit: the one-launch kernel streaming each row only up to its first rejection
 cudaError_t sample_early_exit_launch(SampleParams p, int dtype, cudaStream_t stream);
+// the early exit's one-launch kernel: a thread-block cluster of p.rcs CTAs per batch row (slices of
+// p.rslice elements) that streams a row's positions only up to its first rejection; pdl: launch as a
+// programmatic dependent of the previous launch on the stream
+cudaError_t rows_launch(const SampleParams& p, int dtype, cudaStream_t stream, bool pdl);
+// clusters of cs CTAs of the early exit's one-launch kernel the device holds at once (0: cannot be
+// scheduled), for draft width G
+cudaError_t rows_max_active_clusters(int dtype, int G, int cs, int* out);
 // stream kernel (gamma = 0) then one sampling CTA per row; emitted is the [B] token output
 cudaError_t rows_sample_launch(const SampleParams& p, int dtype, cudaStream_t stream);
 // one CTA per row: the logit threshold of top-k / nucleus standardisation

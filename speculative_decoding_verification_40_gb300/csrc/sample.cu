@@ -34,72 +34,18 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "softmax.cuh"
+#include "verify_common.cuh"
 
 namespace specv {
 
 namespace {
 
-constexpr int kST = kStreamThreads;
-constexpr int kSW = kST / 32;
-constexpr int kR = 4;  // 16-byte vectors per lane in one draw chunk
 constexpr int kShortRowBytes = 8192;  // rows up to this size take the one-launch path
-
-enum : int { kRowInvalid = 1, kRowResid = 2 };
-
-struct RowState {
-  int n, flags;
-  uint32_t err;
-  float uf;      // the final draw's uniform (thread 0 only)
-  int x;         // draft id x_i of this thread's position i = thread index (i < gamma_b)
-  float cp, cq;  // p = 2^(l log2(e)/T + cp), cp = -m_p log2(e)/T - log2 S_p; q likewise (times the lenience)
-  float tt, dt;  // standardisation thresholds of the drawn target / draft row (-inf: none)
-};
-
-// p and w = max(0, p - q) (w = p unless resid) from widened logits: one FFMA and one exp2 per
-// probability; the chunk-mass pass, scalar or packed, computes exactly these.
-template <int kV>
-__device__ __forceinline__ void weights_of(const float (&lt)[kV], const float (&ld)[kV], bool resid,
-                                           const RowState& st, float sc, float (&p)[kV], float (&w)[kV]) {
-#pragma unroll
-  for (int j = 0; j < kV; ++j) {
-    p[j] = fast_exp2(fmaf(masked(lt[j], st.tt), sc, st.cp));
-    w[j] = resid ? fmaxf(p[j] - fast_exp2(fmaf(masked(ld[j], st.dt), sc, st.cq)), 0.f) : p[j];
-  }
-}
-
-// Weights of one lane's kV elements starting at `base` of the drawn row(s): p, and w = max(0, p - q)
-// for a residual draw (w = p otherwise); elements past V weigh 0.  The mass pass and the final scan
-// both use this arithmetic, so they see identical weights.
-template <typename T>
-__device__ __forceinline__ void seg_weights(const T* tr, const T* dr, bool resid, int V, bool vec, int base,
-                                            const RowState& st, float sc, float (&p)[Elems<T>::kVec],
-                                            float (&w)[Elems<T>::kVec]) {
-  constexpr int kV = Elems<T>::kVec;
-  float lt[kV], ld[kV];
-  if (vec && base + kV <= V) {
-    Elems<T>::widen(ldg_stream(tr + base), lt);
-    if (resid) Elems<T>::widen(ldg_stream(dr + base), ld);
-  } else {
-#pragma unroll
-    for (int j = 0; j < kV; ++j) {
-      lt[j] = base + j < V ? Elems<T>::one(tr, base + j) : -INFINITY;
-      ld[j] = (resid && base + j < V) ? Elems<T>::one(dr, base + j) : -INFINITY;
-    }
-  }
-  weights_of<kV>(lt, ld, resid, st, sc, p, w);
-}
-
-template <int kV>
-__device__ __forceinline__ float lane_sum(const float (&w)[kV]) {
-  float s = 0.f;
-#pragma unroll
-  for (int j = 0; j < kV; ++j) s += w[j];
-  return s;
-}
 
 struct DrawSmem {
   float mp[kMaxGamma + 1], sp[kMaxGamma + 1], mq[kMaxGamma + 1], sq[kMaxGamma + 1];
   int acc[kMaxGamma + 1];
+  uint32_t perr[kMaxGamma + 1];  // error bits per position (early-exit validity)
   float2 xl[kMaxGamma];  // logits at the draft tokens (short-row path)
   float2 cs[kMaxRowChunks];  // chunk masses of the drawn row (w, p), gathered by the resolving CTA
   float2 ds[kMaxSlices];     // slice masses of the drawn row (w, p)
@@ -107,57 +53,6 @@ struct DrawSmem {
   int last, pick, mode;
   float t, pre;
 };
-
-// Accept decisions of row b from the slice normalisers: the same arithmetic in every CTA of the row.
-// Row normalisers of one position from its NS slice partials (m_p, S_p, m_q, S_q), combined by one warp
-// in a fixed order, so every caller gets the same values bit for bit.  Every lane returns them.
-// pr: lane r < NS holds slice r's partial (m_p, S_p, m_q, S_q), the other lanes (-inf, 0, -inf, 0).
-__device__ __forceinline__ float4 combine_partials(float4 pr, int NS, float sc) {
-  const float Mp = warp_max_nan(pr.x);
-  const float Mq = warp_max_nan(pr.z);
-  const float tp = (pr.x > -INFINITY && Mp < INFINITY) ? pr.y * fast_exp2((pr.x - Mp) * sc) : 0.f;
-  const float tq = (pr.z > -INFINITY && Mq < INFINITY) ? pr.w * fast_exp2((pr.z - Mq) * sc) : 0.f;
-  float Sp = 0.f, Sq = 0.f;
-  for (int r = 0; r < NS; ++r) {
-    Sp += __shfl_sync(0xffffffffu, tp, r);
-    Sq += __shfl_sync(0xffffffffu, tq, r);
-  }
-  return make_float4(Mp, Sp, Mq, Sq);
-}
-
-__device__ __forceinline__ float4 load_partial(const float4* __restrict__ part_pos, int NS) {
-  float4 pr = make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
-  if ((threadIdx.x & 31) < NS) pr = __ldcg(part_pos + (threadIdx.x & 31));
-  return pr;
-}
-
-__device__ __forceinline__ float4 position_norm(const float4* __restrict__ part_pos, int NS, float sc) {
-  return combine_partials(load_partial(part_pos, NS), NS, sc);
-}
-
-// Accept test of guess i < gamma_b of row b, u_i <= min(1, p(x_i)/q(x_i)) with p(x_i) > 0, from the
-// position's normalisers and the logits at the draft token; err collects what makes the row invalid.
-// x = x_i, ui = u_i and xl = (l_p(x_i), l_q(x_i)) are passed in, so callers can load them early.
-__device__ __forceinline__ int accept_test(const SampleParams& a, float4 nm, int x, float ui, float2 xl,
-                                           uint32_t& err) {
-  if (!(nm.x > -INFINITY && nm.x < INFINITY)) err |= kErrNonfinite;
-  if (!(nm.z > -INFINITY && nm.z < INFINITY)) err |= kErrNonfinite;
-  if (x < 0 || x >= a.V) err |= kErrToken;
-  if (!(ui >= 0.f && ui < 1.f)) err |= kErrArg;
-  if (err) return 0;
-  const float sc = a.scale;
-  const float px = fast_exp2((xl.x - nm.x) * sc) / nm.y;
-  const float qx = fast_exp2((xl.y - nm.z) * sc) / nm.w * a.lq;  // l q(x) (l = 1 unless lenient)
-  const float ratio = px >= qx ? 1.f : px / qx;  // min(1, p/q); q = 0 < p gives 1
-  return (px > 0.f && ui <= ratio) ? 1 : 0;
-}
-
-__device__ __forceinline__ int accept_position(const SampleParams& a, int b, int i, float4 nm, uint32_t& err) {
-  const int x = __ldg(a.ids + (size_t)b * a.G + i);
-  const float ui = __ldg(a.uniforms + (size_t)b * (a.G + 1) + i);
-  const float2 xl = __ldcg(reinterpret_cast<const float2*>(a.ws.xl) + (size_t)b * a.G + i);
-  return accept_test(a, nm, x, ui, xl, err);
-}
 
 // Inputs of the row's decisions that the stream kernel does not write, loaded by the draw kernel before
 // it waits for the stream kernel: thread i <= gamma_b holds x_i and u_i, thread 0 also u_final.
@@ -220,10 +115,33 @@ __device__ RowState decide_row(const SampleParams& a, int b, int gb, const RowIn
       err |= kErrNonfinite;
     }
     sm.acc[i] = err ? -1 : code;
+    // early-exit validity (a.lazy): a logit row after the first rejection counts as never read, so only the
+    // id and uniform checks of those positions stand; the stop position is found after the barrier
+    if (a.lazy) sm.perr[i] = err;
   }
-  if (tid == 0 && !(in.uf >= 0.f && in.uf < 1.f)) err |= kErrArg;
-  if (err) atomicOr(&sm.err, err);
+  if (tid == 0 && !(in.uf >= 0.f && in.uf < 1.f)) {
+    if (a.lazy)
+      atomicOr(&sm.err, kErrArg);
+    else
+      err |= kErrArg;
+  }
+  if (err && !a.lazy) atomicOr(&sm.err, err);
   __syncthreads();
+  if (a.lazy) {
+    if (tid == 0) {
+      int s = gb;  // the first position not accepted: a rejection, an invalid position, or the bonus
+      for (int i = 0; i < gb; ++i) {
+        if (sm.acc[i] != 1) {
+          s = i;
+          break;
+        }
+      }
+      uint32_t e = 0;
+      for (int i = 0; i <= gb; ++i) e |= i <= s ? sm.perr[i] : (sm.perr[i] & (kErrToken | kErrArg));
+      sm.err |= e;
+    }
+    __syncthreads();
+  }
   RowState st = {};
   int n = gb;
   for (int i = 0; i < gb; ++i) {
@@ -499,7 +417,6 @@ __device__ void resolve_row(const SampleParams& a, int b, int gb, const RowState
     for (int k = tid; k < ND * cps; k += kST) dch[k] = make_float2(0.f, 0.f);
   if (tid == 0) {
     a.ws.ticket[b] = 0u;
-    a.ws.stop[b] = 0;
   }
 }
 
@@ -507,86 +424,6 @@ __device__ void resolve_row(const SampleParams& a, int b, int gb, const RowState
 
 // ----------------------------------------------------------------------------- stream kernel
 
-// Online normalisers (m, S) of n logits of one row (and of a second row when has_q), this thread's
-// share: 16-byte vectors when vec, in groups of U per row in flight, then a scalar tail.  raw tracks the
-// NaN-propagating maximum of the raw logits (NaN / +inf detection).
-template <typename T, bool kMask>
-__device__ __forceinline__ void slice_normalisers(const T* __restrict__ tp, const T* __restrict__ dp, bool has_q,
-                                                  int n, bool vec, float sc, float tt, float dt, float& mp,
-                                                  float& sp, float& rp, float& mq, float& sq, float& rq) {
-  constexpr int kV = Elems<T>::kVec;
-  constexpr int U = 4;
-  const int tid = threadIdx.x;
-  int done = 0;
-  if (vec) {
-    const int nv = n / kV;
-    const uint4* t4 = reinterpret_cast<const uint4*>(tp);
-    const uint4* d4 = reinterpret_cast<const uint4*>(dp);
-    int v = tid;
-    if (has_q) {
-      for (; v + (U - 1) * kST < nv; v += U * kST) {
-        uint4 r0[U], r1[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) r0[u] = ldg_stream(t4 + v + u * kST);
-#pragma unroll
-        for (int u = 0; u < U; ++u) r1[u] = ldg_stream(d4 + v + u * kST);
-        online_group<T, U, kMask>(mp, sp, rp, r0, sc, tt);
-        online_group<T, U, kMask>(mq, sq, rq, r1, sc, dt);
-      }
-      if constexpr (sizeof(T) == 2) {
-        // bfloat16: the thread's last (at most U - 1) vectors as one group whose missing vectors read as
-        // -inf, so all of their loads are in flight at once (a 64 KB row of 4000 vectors leaves three)
-        if (v < nv) {
-          const uint4 ninf = make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
-          uint4 r0[U], r1[U];
-#pragma unroll
-          for (int u = 0; u < U; ++u) r0[u] = v + u * kST < nv ? ldg_stream(t4 + v + u * kST) : ninf;
-#pragma unroll
-          for (int u = 0; u < U; ++u) r1[u] = v + u * kST < nv ? ldg_stream(d4 + v + u * kST) : ninf;
-          online_group<T, U, kMask>(mp, sp, rp, r0, sc, tt);
-          online_group<T, U, kMask>(mq, sq, rq, r1, sc, dt);
-        }
-      } else {
-        for (; v < nv; v += kST) {
-          const uint4 r0[1] = {ldg_stream(t4 + v)};
-          const uint4 r1[1] = {ldg_stream(d4 + v)};
-          online_group<T, 1, kMask>(mp, sp, rp, r0, sc, tt);
-          online_group<T, 1, kMask>(mq, sq, rq, r1, sc, dt);
-        }
-      }
-    } else {
-      for (; v + (U - 1) * kST < nv; v += U * kST) {
-        uint4 r0[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) r0[u] = ldg_stream(t4 + v + u * kST);
-        online_group<T, U, kMask>(mp, sp, rp, r0, sc, tt);
-      }
-      if constexpr (sizeof(T) == 2) {
-        if (v < nv) {
-          const uint4 ninf = make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
-          uint4 r0[U];
-#pragma unroll
-          for (int u = 0; u < U; ++u) r0[u] = v + u * kST < nv ? ldg_stream(t4 + v + u * kST) : ninf;
-          online_group<T, U, kMask>(mp, sp, rp, r0, sc, tt);
-        }
-      } else {
-        for (; v < nv; v += kST) {
-          const uint4 r0[1] = {ldg_stream(t4 + v)};
-          online_group<T, 1, kMask>(mp, sp, rp, r0, sc, tt);
-        }
-      }
-    }
-    done = nv * kV;
-  }
-  for (int k = done + tid; k < n; k += kST) {
-    float f[1] = {Elems<T>::one(tp, k)};
-    online<1, kMask>(mp, sp, rp, f, sc, tt);
-    if (has_q) {
-      f[0] = Elems<T>::one(dp, k);
-      online<1, kMask>(mq, sq, rq, f, sc, dt);
-    }
-  }
-}
 
 // Block merge of the threads' normalisers in a fixed order (identical for p and q): warp shuffles, then
 // thread 0 over the warps.  Thread 0 returns the block's (m_p, S_p, m_q, S_q) and raw maximum.
@@ -626,30 +463,21 @@ template <typename T, bool kMask>
 __global__ void __launch_bounds__(kStreamThreads, 4) verify_stream_kernel(const SampleParams a) {
   __shared__ float red[4][kSW];
   __shared__ float rawr[kSW];
-  __shared__ int last;
   const int tid = threadIdx.x;
   // Launched as a programmatic dependent of whatever precedes it on the stream (the previous call's
-  // draw kernel, the previous early-exit position, or the caller's kernel that wrote the logits): its
-  // CTAs may be resident early, and read nothing until that grid has finished and its writes are
-  // visible.  Only then may the draw kernel be scheduled (it reads the row inputs before its own wait).
+  // draw kernel, or the caller's kernel that wrote the logits): its CTAs may be resident early, and read
+  // nothing until that grid has finished and its writes are visible.  Only then may the draw kernel be
+  // scheduled (it reads the row inputs before its own wait).
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
   const int NS = a.nslices;
   const int s = blockIdx.x % NS;
   const int G1 = a.G + 1;
-  int b, i;
-  if (a.step) {  // early exit: position step - 1 of row b, unless the row already stopped
-    b = blockIdx.x / NS;
-    i = a.step - 1;
-  } else {
-    const int p = blockIdx.x / NS;
-    b = p / G1;
-    i = p - b * G1;
-  }
-  const int pos = b * G1 + i;
+  const int pos = blockIdx.x / NS;
+  const int b = pos / G1;
+  const int i = pos - b * G1;
   const int gb = a.draft_len ? __ldg(a.draft_len + b) : a.G;
   if (gb < 0 || gb > a.G || i > gb) return;  // invalid length (the draw kernel reports it) or padding
-  if (a.step && __ldcg(a.ws.stop + b) != 0) return;  // the previous positions' decisions (waited for above)
   const bool has_q = i < gb;
   const float sc = a.scale;
   const int lo = s * a.slice;
@@ -676,26 +504,6 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_stream_kernel(const 
     const bool bad = !(raw < INFINITY);  // NaN or +inf in this slice
     reinterpret_cast<float4*>(a.ws.part)[(size_t)pos * NS + s] =
         make_float4(bad ? NAN : nrm.x, nrm.y, bad ? NAN : nrm.z, nrm.w);
-  }
-  if (!a.step) return;
-  // early exit: the last CTA of (b, i) decides guess i -- the draw kernel's test, same arithmetic -- and
-  // stops the row at a rejection, an invalid position or the bonus position gamma_b
-  if (tid == 0 || tid == 32) __threadfence();
-  __syncthreads();
-  if (tid == 0) last = atomicAdd(a.ws.ticket + b, 1u) == static_cast<unsigned>(NS - 1);
-  __syncthreads();
-  if (!last || tid >= 32) return;
-  __threadfence();
-  const float4 nm = position_norm(reinterpret_cast<const float4*>(a.ws.part) + (size_t)pos * NS, NS, sc);
-  if (tid == 0) {
-    a.ws.ticket[b] = 0u;
-    bool stop = i == gb;
-    if (!stop) {
-      uint32_t err = 0;
-      const int code = accept_position(a, b, i, nm, err);
-      stop = err != 0 || code == 0;
-    }
-    if (stop) a.ws.stop[b] = i + 1;
   }
 }
 
@@ -945,7 +753,7 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_short_kernel(const S
 // The one-launch path applies to 16-byte aligned rows of at most kShortRowBytes with one stream slice and
 // one draw slice per row.
 static bool short_rows(const SampleParams& p, size_t esz) {
-  return p.vec != 0 && p.step == 0 && static_cast<size_t>(p.V) * esz <= static_cast<size_t>(kShortRowBytes) &&
+  return p.vec != 0 && static_cast<size_t>(p.V) * esz <= static_cast<size_t>(kShortRowBytes) &&
          p.nslices == 1 && p.ndslices == 1;
 }
 
@@ -955,6 +763,14 @@ static bool short_rows(const SampleParams& p, size_t esz) {
 static bool pdl_first() {
   const char* env = std::getenv("SPECVERIFY_PDL");
   return !(env && std::atoi(env) == 0);
+}
+
+// The early exit's form from the environment: 1 = the one-launch kernel, 2 = the two-kernel path, 0 = unset.
+static int form_env(const char* name) {
+  const char* env = std::getenv(name);
+  if (!env) return 0;
+  const int v = std::atoi(env);
+  return v == 1 || v == 2 ? v : 0;
 }
 
 // A row's draw CTAs form one cluster when there are 2 to 8 of them (the portable cluster size) and the
@@ -990,24 +806,25 @@ static cudaError_t launch_draw(const SampleParams& p, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, verify_draw_kernel<T>, q);
 }
 
+// The early exit runs the one-launch kernel, which streams a row's positions one after the other and
+// stops at the first rejection, when one position of the whole batch is large enough for the bytes it
+// skips to outweigh its per-position latency: at least 64 MB over the batch's target and draft rows
+// (c3: 256 x 2 rows of 608 KB, 193 vs 285 us for all positions; c4: 131 MB, 127 vs 134 us).  Smaller
+// batches (c2: 33 MB, 76 vs 61 us) take the two-kernel all-positions path, whose draw then takes the
+// decisions with early-exit validity (logit rows after the first rejection do not count).  Both give
+// the early exit's results.  SPECVERIFY_EARLY_FORM=1 / 2 forces the one-launch / two-kernel form.
+static bool early_one_launch(const SampleParams& p, int dtype) {
+  if (p.rcs <= 0) return false;  // no cluster plan for this shape on this device
+  const int f = form_env("SPECVERIFY_EARLY_FORM");
+  if (f) return f == 1;
+  const long long position_bytes = 2LL * p.B * p.V * (dtype == 0 ? 4 : 2);
+  return position_bytes >= (64LL << 20);
+}
+
 cudaError_t sample_early_exit_launch(SampleParams p, int dtype, cudaStream_t stream) {
-  for (int i = 0; i <= p.G; ++i) {
-    p.step = i + 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>((long long)p.B * p.nslices));
-    cfg.blockDim = dim3(kStreamThreads);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = (i > 0 || pdl_first()) ? 1 : 0;  // each position's launch overlaps the previous one's tail
-    const cudaError_t e = dtype == 0 ? cudaLaunchKernelEx(&cfg, verify_stream_kernel<float, false>, p)
-                                     : cudaLaunchKernelEx(&cfg, verify_stream_kernel<__nv_bfloat16, false>, p);
-    if (e != cudaSuccess) return e;
-  }
-  p.step = 0;
-  return dtype == 0 ? launch_draw<float>(p, stream) : launch_draw<__nv_bfloat16>(p, stream);
+  if (early_one_launch(p, dtype)) return rows_launch(p, dtype, stream, pdl_first());
+  p.lazy = 1;
+  return sample_launch(p, dtype, 3, stream);
 }
 
 // ----------------------------------------------------------------------------- row sampler
@@ -1387,7 +1204,7 @@ static cudaError_t launch_first(K kernel, dim3 grid, const SampleParams& p, cuda
 
 template <typename T, bool kMask>
 static cudaError_t sample_launch_t(const SampleParams& p, int phases, cudaStream_t stream) {
-  if (phases == 3 && short_rows(p, sizeof(T)))
+  if (phases == 3 && !p.lazy && short_rows(p, sizeof(T)))
     return launch_first(verify_short_kernel<T, kMask>, dim3(static_cast<unsigned>(p.B)), p, stream);
   const dim3 g1(static_cast<unsigned>((long long)p.B * (p.G + 1) * p.nslices));
   if (phases & 1) {

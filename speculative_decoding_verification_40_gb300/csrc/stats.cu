@@ -78,11 +78,6 @@ __device__ __forceinline__ void write_stats(const VerifyParams& a, size_t o, flo
   if (a.resid) a.resid[o] = z;
 }
 
-__device__ __forceinline__ void dsmem_st_v4(uint32_t addr, float a, float b, float c, float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
-
 }  // namespace
 
 template <typename T>

@@ -174,8 +174,10 @@ def test_cluster_sizes_agree(S, monkeypatch):
 
 
 @pytest.mark.parametrize("k", [1, 4])
-def test_split_phases_equal_the_whole_call(S, k):
-    """spec_verify_sample_stream then spec_verify_sample_draw is exactly spec_verify_sample."""
+def test_split_phases_agree_with_the_whole_call(S, k):
+    """spec_verify_sample_stream then spec_verify_sample_draw (the two-kernel form) and spec_verify_sample
+    (one launch) split the vocabulary differently, so their float32 sums round differently: both match the
+    oracle, and their tokens are identical on every row that is not a boundary draw."""
     w = W.make(k, device="cuda", B=64 if k == 4 else None)
     em, na = S.verify_sample(w.target, w.draft, w.ids, w.uniforms, w.T, w.draft_len)
     em2 = torch.full_like(em, 7)
@@ -185,4 +187,11 @@ def test_split_phases_equal_the_whole_call(S, k):
     S.verify_sample(w.target, w.draft, w.ids, w.uniforms, w.T, w.draft_len, emitted=em2, n_accepted=na2,
                     phase="draw")
     assert S.check_status() == 0
-    assert torch.equal(em, em2) and torch.equal(na, na2)
+    h = host_inputs(w)
+    n, flagged, mism = compare_sample(w, em, na, h)
+    assert not mism, mism[:3]
+    n2, flagged2, mism2 = compare_sample(w, em2, na2, h)
+    assert not mism2, mism2[:3]
+    assert flagged == flagged2
+    same = [b for b in range(w.B) if b not in set(flagged)]
+    assert torch.equal(em[same], em2[same]) and torch.equal(na[same], na2[same])
