@@ -263,6 +263,13 @@ def cpu_oracle_rate(w: W.Workload, rows: int, procs: int, pool=None, gpu=None) -
 
 # ----------------------------------------------------------------------------- arms
 
+def early_form(w: W.Workload) -> str:
+    """Which form spec_verify_sample_early_exit takes for this batch (the library's rule: one launch when a
+    position of the batch, 2 B V logits, is at least 64 MB)."""
+    esz = 4 if w.dtype == "f32" else 2
+    return "one-launch cluster kernel" if 2 * w.B * w.V * esz >= (64 << 20) else "two-kernel path, early-exit validity"
+
+
 def c0_latency(S, dev, stream, ncalls: int = 50, reps: int = 20) -> dict:
     """c0 (B=1, gamma=4, V=1024): microseconds per call over independent calls, launched one by one and
     replayed from a captured CUDA graph (the library's calls are launches only, so they capture)."""
@@ -474,9 +481,18 @@ def run_ours(a, rank, world, dist):
 
             ms = time_device(call2, max(20, a.steps), 5, stream)
             gbs = w2.read_once_bytes() / (ms * 1e-3) / 1e9
+
+            def early2():
+                t, d = copies2[turn2[0] % len(copies2)]
+                turn2[0] += 1
+                S.verify_sample(t, d, w2.ids, w2.uniforms, w2.T, w2.draft_len, workspace=ws2, phase="early_exit")
+
+            ems = time_device(early2, max(20, a.steps), 5, stream)
             also[w2.name] = {"ms_per_call": round(ms, 5), "positions_per_s": w2.positions() / (ms * 1e-3),
                              "rows_per_s": w2.B / (ms * 1e-3), "GB_per_s": round(gbs, 1),
                              "frac_of_measured_hbm": round(gbs / peak, 4),
+                             "early_exit_ms_per_call": round(ems, 5),
+                             "early_exit_form": early_form(w2),
                              "l2": "three copies of the logits used in turn"}
             del w2, copies2
         assert S.check_status(ws2) == 0
@@ -532,7 +548,7 @@ def run_ours(a, rank, world, dist):
                      "thresholds_GB_per_s": (w.B * (2 * w.gamma + 1)) * w.V * esz / (topp_ms * 1e-3) / 1e9,
                      "masked_verify_ms_per_call": masked_ms,
                      "lenient_verify_ms_per_call": lenient_ms,
-                     "early_exit_ms_per_call": early_ms,
+                     "early_exit_ms_per_call": early_ms, "early_exit_form": early_form(w),
                      "early_exit_rows_read": early_rows, "all_positions_rows_read": w.B + 2 * pos,
                      "early_exit_GB_per_s": early_rows * w.V * esz / (early_ms * 1e-3) / 1e9,
                      "sampler_rows": int(s_logits.shape[0]), "sampler_ms_per_call": sampler_ms,

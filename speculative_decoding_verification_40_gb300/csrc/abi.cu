@@ -78,18 +78,29 @@ int device_sms();
 constexpr int kMinSlice = 4096;
 
 // Vocabulary elements per sampling CTA and logit row: 64 KB of the row, at least V/32 so a row has
-// at most 32 slices.  `positions` > 0 (the verification's B (gamma + 1)): a batch that would give
-// fewer than two stream CTAs per SM has its slices halved, down to kMinSlice elements, so that a
-// latency-bound small batch still spreads over the GPU (c1, B = 8 and gamma = 4 over V = 32128:
-// 320 CTAs of 4096 elements instead of 40 of 32768).  SPECVERIFY_SLICE (elements) overrides within the
-// same limits.
+// at most 32 slices.  `positions` > 0 (the verification's B (gamma + 1)):
+//  - a batch that would give fewer than two stream CTAs per SM has its slices halved, down to kMinSlice
+//    elements, so that a latency-bound small batch still spreads over the GPU (c1, B = 8 and gamma = 4
+//    over V = 32128: 320 CTAs of 4096 elements instead of 40 of 32768);
+//  - a batch whose grid fits one wave of four CTAs per SM, with at least three per SM, when its slices are
+//    larger (up to 256 KB of a row, the most a draw-chunk count allows) takes the largest such slice: the
+//    whole stream pass then starts at once and has no partially filled last wave (c2, B = 64, gamma = 8,
+//    V = 128256: 576 CTAs of a whole 250 KB row, 57.9 us per call against 60.4 us for 2304 CTAs of 64 KB).
+// SPECVERIFY_SLICE (elements) overrides within the same limits.
 int sample_slice(int V, int dtype, long long positions = 0) {
   const int chunk = 4 * 32 * (dtype == SPEC_F32 ? 4 : 8);  // elements per draw chunk (4 x 32 lanes x 16 B)
   const int esz = dtype == SPEC_F32 ? 4 : 2;
   int slice = specv::kStreamSliceBytes / esz;
   if (positions > 0) {
-    const long long want = 2LL * (device_sms() > 0 ? device_sms() : 152);
-    while (slice / 2 >= kMinSlice && positions * ((V + slice - 1) / slice) < want) slice /= 2;
+    const long long sms = device_sms() > 0 ? device_sms() : 152;
+    while (slice / 2 >= kMinSlice && positions * ((V + slice - 1) / slice) < 2 * sms) slice /= 2;
+    for (int big = specv::kMaxChunksPerSlice * chunk; big > slice; big /= 2) {
+      const long long ctas = positions * ((V + big - 1) / big);
+      if (ctas <= 4 * sms && ctas >= 3 * sms) {
+        slice = big;
+        break;
+      }
+    }
   }
   if (const char* env = std::getenv("SPECVERIFY_SLICE")) {
     const int want = std::atoi(env);
