@@ -146,14 +146,17 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# The sources the stream kernel (verify_stream_kernel, the roofline's kernel) is built from.
+STREAM_KERNEL_SOURCES = ("common.cuh", "kernels.h", "sample.cu", "softmax.cuh", "verify_common.cuh")
+
+
 def kernel_sources_digest() -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verification_40_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in STREAM_KERNEL_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
@@ -262,6 +265,32 @@ def cpu_oracle_rate(w: W.Workload, rows: int, procs: int, pool=None, gpu=None) -
 
 
 # ----------------------------------------------------------------------------- arms
+
+def gpu_local_cpus(index: int):
+    """The host CPUs local to CUDA device `index` and their NUMA node, from the PCI device's sysfs entries
+    (local_cpulist, numa_node), restricted to the CPUs this process may use; None if unknown."""
+    try:
+        p = torch.cuda.get_device_properties(index)
+        dom, bus, devn = (getattr(p, k, None) for k in ("pci_domain_id", "pci_bus_id", "pci_device_id"))
+        if None in (dom, bus, devn):
+            return None
+        base = f"/sys/bus/pci/devices/{dom:04x}:{bus:02x}:{devn:02x}.0"
+        with open(base + "/local_cpulist") as f:
+            spec = f.read().strip()
+        with open(base + "/numa_node") as f:
+            node = int(f.read().strip())
+        cpus = set()
+        for part in spec.split(","):
+            if "-" in part:
+                lo, hi = part.split("-")
+                cpus.update(range(int(lo), int(hi) + 1))
+            elif part:
+                cpus.add(int(part))
+        cpus &= os.sched_getaffinity(0)
+        return {"cpus": cpus, "node": node} if cpus else None
+    except (OSError, ValueError, AttributeError, RuntimeError):
+        return None
+
 
 def early_form(w: W.Workload) -> str:
     """Which form spec_verify_sample_early_exit takes for this batch (the library's rule: one launch when a
@@ -391,13 +420,23 @@ def run_ours(a, rank, world, dist):
     peak, peak_kind = hbm_peak()
     traffic = recorded_traffic(w.name)
 
-    # end to end through the public API: pinned host inputs -> device -> verify -> host results
-    host = {n: getattr(w, n).cpu().pin_memory() for n in ("target", "draft", "ids", "uniforms")}
-    if w.draft_len is not None:
-        host["draft_len"] = w.draft_len.cpu().pin_memory()
+    # end to end through the public API: pinned host inputs -> device -> verify -> host results.  The
+    # pinned buffers are allocated from the CPUs local to the GPU (so their pages sit on its host NUMA
+    # node), unless --e2e-numa any.
+    local = gpu_local_cpus(dev.index) if a.e2e_numa == "local" else None
+    saved = os.sched_getaffinity(0) if local else None
+    if local:
+        os.sched_setaffinity(0, local["cpus"])
+    try:
+        host = {n: getattr(w, n).cpu().pin_memory() for n in ("target", "draft", "ids", "uniforms")}
+        if w.draft_len is not None:
+            host["draft_len"] = w.draft_len.cpu().pin_memory()
+        out_em = torch.empty(w.B, w.gamma + 1, dtype=torch.int32).pin_memory()
+        out_na = torch.empty(w.B, dtype=torch.int32).pin_memory()
+    finally:
+        if saved:
+            os.sched_setaffinity(0, saved)
     dev_in = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
-    out_em = torch.empty(w.B, w.gamma + 1, dtype=torch.int32).pin_memory()
-    out_na = torch.empty(w.B, dtype=torch.int32).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_em.numel() * 4 + out_na.numel() * 4
 
@@ -474,10 +513,15 @@ def run_ours(a, rank, world, dist):
             copies2 = rotation(w2)
             turn2 = [0]
 
+            em2 = torch.empty(w2.B, w2.gamma + 1, dtype=torch.int32, device=dev)
+            na2 = torch.empty(w2.B, dtype=torch.int32, device=dev)
+
+            # output buffers passed in, so the loop times the library's launches, not the binding's allocations
             def call2():
                 t, d = copies2[turn2[0] % len(copies2)]
                 turn2[0] += 1
-                S.verify_sample(t, d, w2.ids, w2.uniforms, w2.T, w2.draft_len, workspace=ws2)
+                S.verify_sample(t, d, w2.ids, w2.uniforms, w2.T, w2.draft_len, emitted=em2, n_accepted=na2,
+                                workspace=ws2)
 
             ms = time_device(call2, max(20, a.steps), 5, stream)
             gbs = w2.read_once_bytes() / (ms * 1e-3) / 1e9
@@ -485,7 +529,8 @@ def run_ours(a, rank, world, dist):
             def early2():
                 t, d = copies2[turn2[0] % len(copies2)]
                 turn2[0] += 1
-                S.verify_sample(t, d, w2.ids, w2.uniforms, w2.T, w2.draft_len, workspace=ws2, phase="early_exit")
+                S.verify_sample(t, d, w2.ids, w2.uniforms, w2.T, w2.draft_len, emitted=em2, n_accepted=na2,
+                                workspace=ws2, phase="early_exit")
 
             ems = time_device(early2, max(20, a.steps), 5, stream)
             also[w2.name] = {"ms_per_call": round(ms, 5), "positions_per_s": w2.positions() / (ms * 1e-3),
@@ -537,7 +582,10 @@ def run_ours(a, rank, world, dist):
                      "kernel_ms": stream_ms,
                      "algorithmic_bytes_per_launch": nbytes},
         "e2e": {"value": e2e_units / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "h2d_GB_per_s_upper_bound": round(h2d / (e2e_ms * 1e-3) / 1e9, 1),
+                "pinned_buffers": (f"allocated from the GPU's local CPUs (host NUMA node {local['node']})" if local
+                                   else "allocated without CPU placement")},
         "gpu_launches": 2 * a.steps,
         "clocks": clocks,
         "variants": {"greedy_ms_per_call": greedy_ms,
@@ -651,6 +699,8 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=512)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-also", action="store_true")
+    ap.add_argument("--e2e-numa", choices=["local", "any"], default="local",
+                    help="where the e2e step's pinned host buffers are allocated from")
     ap.add_argument("--batch", type=int, default=0,
                     help="rows of the workload (same recipe; default: the workload's own B) -- for profiling "
                          "a smaller case of the same kernels")
