@@ -65,6 +65,52 @@ def test_topk_threshold_invalid_and_degenerate_rows(S):
     assert np.isnan(thr[0]) and np.isnan(thr[1]) and thr[2] == -np.inf and thr[3] == np.float32(1.5)
 
 
+def _long_rows(V, dtype, offset):
+    """Rows of V logits that steer the threshold kernel down each of its paths.  The kernel bins the row
+    against the max R of its first sixteenth (at least 4096 logits) and sets aside the logits above R;
+    it falls back to binning against the true max when more than 2048 lie above R, or (nucleus) when the
+    max lies 10 or more log2 units above R."""
+    R = 12
+    l = _random_rows(R, V, dtype, 77, offset)
+    pre = max(4096, V // 16)
+    l[1, V - 3] = float("nan")                                   # NaN late in the row
+    l[2, V // 2 + 1] = float("inf")                              # +inf late in the row
+    l[3, :] = float("-inf")                                      # nothing finite
+    l[4, :] = 1.5                                                # all tied: a bin past the sort buffer
+    l[5, :] = float("-inf")                                      # 40 finite logits, all after the prefix
+    l[5, V - 40:] = 0.25 * torch.arange(40, device="cuda", dtype=l.dtype)
+    l[6, :] = float("-inf")                                      # a single finite logit
+    l[6, V - 1] = -2.0
+    l[7] = (l[7].float() + W.zipf_log_prior(V, 1.1, "cuda")).to(l.dtype)  # the max inside the prefix
+    l[8] = torch.linspace(-8.0, 8.0, V, device="cuda").to(l.dtype)         # increasing: overflow past 2048
+    l[9, pre:pre + 30] = 14.0 + torch.arange(30, device="cuda", dtype=l.dtype) * 0.125  # a peak after the
+    l[10, :pre] -= 30.0                                          # prefix 30 below the rest: nucleus fallback
+    l[11, :pre] = float("-inf")                                  # empty prefix
+    return l
+
+
+@pytest.mark.parametrize("V,dtype,offset", [(150001, "bf16", 0), (100000, "f32", 0), (70001, "f32", 1),
+                                           (262144, "f32", 0), (9000, "bf16", 0)])
+def test_thresholds_on_every_selection_path(S, V, dtype, offset):
+    """Top-k exact and nucleus exact outside flagged rows against the oracle on rows that end the selection
+    inside the logits above the provisional max, inside the histogram, in the radix selection, and in both
+    fallbacks; NaN / +inf rows give NaN, rows with nothing finite -inf (top-k) or NaN (nucleus)."""
+    l = _long_rows(V, dtype, offset)
+    h, dt = _rows_np(l)
+    for k in (1, 50, 9000):
+        thr = S.topk_threshold(l, k).cpu().numpy()
+        assert np.isnan(thr[1]) and np.isnan(thr[2]) and thr[3] == -np.inf
+        for r in [0] + list(range(4, l.shape[0])):
+            assert np.float32(thr[r]) == np.float32(O.topk_threshold(O.widen(h[r], dt), k)), (k, r, thr[r])
+    for top_p, T in ((0.5, 1.0), (0.9, 0.7), (0.999, 1.3), (1.0, 1.0)):
+        thr = S.topp_threshold(l, T, top_p).cpu().numpy()
+        assert np.isnan(thr[1]) and np.isnan(thr[2]) and np.isnan(thr[3])
+        for r in [0] + list(range(4, l.shape[0])):
+            tau, flag = O.topp_threshold(O.widen(h[r], dt), float(np.float32(T)), float(np.float32(top_p)))
+            if not flag:
+                assert np.float32(thr[r]) == np.float32(tau), (top_p, r, thr[r], tau)
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("top_p,T", [(0.5, 1.0), (0.9, 0.7), (0.99, 1.3), (0.05, 1.0), (1.0, 1.0)])
 def test_topp_threshold_matches_oracle(S, dtype, top_p, T):
