@@ -9,19 +9,28 @@
 // logit threshold tau per row (ties at tau are all kept); the verification and
 // sampling entry points take tau and treat logits below it as -inf.
 //
-// One CTA per row.  Pass 0 takes the row max M.  Pass 1 histograms the row
-// over 2048 bins of the distance from the max, floor((M - l) c) (c = 48 per
-// unit of log2 probability, so a bin is an interval of logits and a lower bin
-// holds larger logits; logits more than 42.6 units down, whose nucleus weight
-// is below the 2^-40 fixed point, share the last bin, summed in registers):
-// top-k counts elements, nucleus sums the weights 2^((l - M) log2(e)/T) in 2^-40
-// fixed point (exact, order-independent integer adds: the same result in every
-// run).  The bin holding the k-th element / the running mass top_p * total is
-// found by a block scan; pass 2 gathers that bin's logits into shared memory
-// and sorts them (bitonic), and the threshold is read off the sorted bin.  If
-// the bin holds more than 8192 logits, an exact radix selection over the
-// order-preserving 32-bit keys of the bin's logits (11 + 11 + 10 bits, one pass
-// each) takes over.
+// One CTA per row.  Logits are binned by their distance from a reference R,
+// floor((R - l) c) over 2048 bins (c = 48 per unit of log2 probability, so a
+// bin is an interval of logits and a lower bin holds larger logits; logits
+// more than 42.6 units down, whose nucleus weight is below the 2^-40 fixed
+// point, share the last bin, counted in registers).  Nucleus masses are sums
+// of the weights 2^((l - R) log2(e)/T) in 2^-40 fixed point: exact,
+// order-independent integer adds, the same result in every run.
+//   Rows of at most 128 KB: R is the row max (pass 0); pass 1 counts (top-k)
+//   or sums the fixed-point weights (nucleus) per bin; the bin holding the
+//   k-th logit / the running mass top_p * total is found by a block scan; pass
+//   2 gathers it, and the threshold is read off its logits in descending
+//   order.
+//   Longer rows: R is the max of the row's first sixteenth, so pass 1 (counts
+//   per bin, the logits above R set aside) also finds the true max, and the
+//   row is read twice in all.  Top-k proceeds as above; the nucleus brackets
+//   the bins its threshold can lie in from the counts (a bin's count bounds its
+//   mass within 1.6 %), gathers them in pass 2 while summing every weight in
+//   float, and takes the threshold the exact fixed-point sums give wherever the
+//   float sums' error bounds leave one candidate (else one exact pass decides).
+// A selected bin of more than 4096 logits takes an exact radix selection over
+// the order-preserving 32-bit keys of its logits (11 + 11 + 10 bits, one pass
+// each).
 #include <cuda_bf16.h>
 
 #include "../../include/spec_verify.h"
@@ -282,6 +291,18 @@ __device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v
   return t;
 }
 
+// Block-wide maximum of the threads' values; every thread gets it.
+__device__ __forceinline__ unsigned int block_max_u32(unsigned int v, unsigned long long* wsum) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = __reduce_max_sync(0xffffffffu, v);
+  if (lane == 0) wsum[warp] = v;
+  __syncthreads();
+  unsigned int m = 0;
+  for (int w = 0; w < kTW; ++w) m = max(m, static_cast<unsigned int>(wsum[w]));
+  __syncthreads();
+  return m;
+}
+
 // The first index of s[0, n) (n <= kPer * kTT, largest logit first) at which the running sum of units from
 // index 0 reaches need, 1 <= need <= the sum over s[0, n); every thread gets it.
 template <int kPer, typename U>
@@ -312,6 +333,68 @@ __device__ int first_reaching(const float* s, int n, unsigned long long need, U&
   }
   __syncthreads();
   const int r = *out;
+  __syncthreads();
+  return r;
+}
+
+// Descending order of n <= kTT gathered logits without a sorting network: thread t counts the logits that
+// come before cand[t] (larger, or equal with a smaller index) and stores cand[t] at that position of out.
+// One barrier.
+__device__ __forceinline__ void rank_sort(const float* cand, int n, float* out) {
+  const int t = threadIdx.x;
+  if (t < n) {
+    const float f = cand[t];
+    int r = 0;
+    for (int j = 0; j < n; ++j) {
+      const float g = cand[j];
+      r += (g > f || (g == f && j < t)) ? 1 : 0;
+    }
+    out[r] = f;
+  }
+  __syncthreads();
+}
+
+// Over s[0, n) (n <= kPer * kTT, largest first) with units(s[i]): the first index whose running sum reaches
+// need_a, the same for need_b (-1 where the whole sum stays below), and the whole sum.  Every thread gets
+// them.  One block scan.
+struct Reach {
+  int a, b;
+  unsigned long long total;
+};
+
+template <int kPer, typename U>
+__device__ Reach reach_two(const float* s, int n, unsigned long long need_a, unsigned long long need_b, U&& units,
+                           unsigned long long* wsum, Reach* out) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    out->a = -1;
+    out->b = -1;
+  }
+  unsigned long long v[kPer], local = 0;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int i = tid * kPer + j;
+    v[j] = i < n ? units(s[i]) : 0ull;
+    local += v[j];
+  }
+  const unsigned long long incl_w = warp_incl_u64(local, lane);
+  if (lane == 31) wsum[warp] = incl_w;
+  __syncthreads();
+  unsigned long long run = 0, total = 0;
+  for (int w = 0; w < kTW; ++w) {
+    if (w < warp) run += wsum[w];
+    total += wsum[w];
+  }
+  run += incl_w - local;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int i = tid * kPer + j;
+    if (run < need_a && run + v[j] >= need_a) out->a = i;
+    if (run < need_b && run + v[j] >= need_b) out->b = i;
+    run += v[j];
+  }
+  __syncthreads();
+  const Reach r{out->a, out->b, total};
   __syncthreads();
   return r;
 }
@@ -458,35 +541,25 @@ __device__ Bracket nucleus_bracket(const Hist& h, unsigned long long base, float
   return Bracket{f, l, n};
 }
 
-// Compensated (Kahan) running sum: s + c carries the sum of the added values to within a few float ulps of
-// the total, whatever their number.
-struct Kahan {
-  float s = 0.f, c = 0.f;
-  __device__ __forceinline__ void add(float x) {
-    const float y = x - c;
-    const float t = s + y;
-    c = (t - s) - y;
-    s = t;
-  }
-};
-
 // Top-k (kTopP = false: k) or nucleus (kTopP = true: top_p, temperature scale) threshold of one row.
 //
-// The distance bins need a reference at or above the logits they hold, and the nucleus weights need one
-// too; for a long row the row max would cost a pass of its own, so the reference is R, the max of the
-// row's first sixteenth.  Pass 1 counts the logits per distance bin and sets aside the few above R (the
-// "overflow", at most kOver); these rank above every binned logit, so the selection walks the sorted
-// overflow first, then the bins from the top.
-//   top-k: the bin of the k-th logit from the counts; pass 2 gathers it, and a sort (or, past kCap
-//     logits, the radix selection) finds the logit.
+// kWhole (rows of at most kSampleRowBytes): R is the row max, taken by a pass of its own; then pass 1 and
+// the gather as in the file comment (the nucleus weighted per bin at once).
+// Otherwise the distance bins and the nucleus weights take as reference R the max of the row's first
+// sixteenth.  Pass 1 counts the logits per distance bin and sets aside the few above R (the "overflow", at
+// most kOver); these rank above every binned logit, so the selection walks the sorted overflow first, then
+// the bins from the top.
+//   top-k: the bin of the k-th logit from the counts; pass 2 gathers it, and the logit's rank among the
+//     gathered (or, past kCap logits, the radix selection) gives the threshold.
 //   nucleus: a bin's count bounds its mass within about 1.6 %, so the counts bracket the bins the running
 //     mass top_p * total can end in; pass 2 gathers the logits of a logit interval holding those bins and
-//     sums every weight in floating point (compensated): the total, and the mass above the interval.
-//     The candidates' exact fixed-point weights are then scanned for the running mass top_p * total,
-//     taken at both ends of the sums' error bounds: if both ends stop at the same logit, that logit is the
-//     threshold the exact fixed-point sums give; otherwise (rare) a pass of exact fixed-point sums
-//     decides.  A bracket of more than kCap logits (top_p within a few percent of 1) takes the weighted
-//     histogram instead: exact fixed-point masses per bin, then the gather.
+//     sums every weight in float (compensated for the many below the interval): the total, and the mass
+//     above the interval.  The candidates' exact fixed-point weights are then scanned, in descending
+//     order, for the running mass top_p * total taken at both ends of the sums' error bounds: if both ends
+//     stop at the same logit, that logit is the threshold the exact fixed-point sums give; otherwise
+//     (rare: 1 or 2 of 1536 c3 rows) a pass of exact fixed-point sums decides.  A bracket of more than
+//     kCap logits (top_p within a few percent of 1) takes the weighted histogram instead: exact
+//     fixed-point masses per bin, then the gather.
 // So a long row is read twice, apart from its prefix and those fallbacks.  If more than kOver logits lie
 // above R, or the nucleus weights of the overflow could leave the fixed point (M - R above kOverUnits),
 // pass 1 is run again against R = M, where nothing lies above the reference.
@@ -505,6 +578,7 @@ __global__ void __launch_bounds__(kTT, 3) threshold_kernel(const void* __restric
   __shared__ float red[kTW];
   __shared__ Pick pk;
   __shared__ Bracket bk;
+  __shared__ Reach rc;
   __shared__ int cnt, nover, sel;
   const int tid = threadIdx.x;
   const T* row = reinterpret_cast<const T*>(logits) + (size_t)blockIdx.x * V;
@@ -615,53 +689,75 @@ __global__ void __launch_bounds__(kTT, 3) threshold_kernel(const void* __restric
       // half a bin of margin at each end for the bins' rounding
       const float x_hi = R - (static_cast<float>(br.first) - 0.5f) / b48;
       const float x_lo = R - (static_cast<float>(br.last) + 1.5f) / b48;
-      // pass 2: the interval's logits into shared memory; the weights of every logit at or below R, and of
-      // those above the interval, summed in floating point
-      Kahan tot, above;
+      // pass 2: the interval's logits into shared memory, and every weight summed in float: below the
+      // interval (the common case: one comparison, a compensated sum), inside it, and above it up to R
+      // (plain sums, with their term counts; the logits above R are the overflow, whose exact mass is O;
+      // -inf weighs 0)
+      float lo_s = 0.f, lo_c = 0.f, tin = 0.f, tab = 0.f;
+      unsigned int nin = 0, nab = 0;
       for_each_logit<T>(row, V, vv, [&](float f) {
-        if (f <= R) {
-          const float w = fast_exp2(fmaf(f, scale, nm));
-          tot.add(w);
-          if (f > x_hi) {
-            above.add(w);
-          } else if (f >= x_lo) {
-            const int at = atomicAdd(&cnt, 1);
-            if (at < kCap) cand[at] = f;
+        const float w = fast_exp2(fmaf(f, scale, nm));
+        if (f >= x_lo) {
+          if (f <= R) {
+            if (f > x_hi) {
+              tab += w;
+              ++nab;
+            } else {
+              tin += w;
+              ++nin;
+              const int at = atomicAdd(&cnt, 1);
+              if (at < kCap) cand[at] = f;
+            }
           }
+        } else {  // Kahan: lo_s + lo_c holds the sum to within a few ulps of it
+          const float y = w - lo_c;
+          const float t = lo_s + y;
+          lo_c = (t - lo_s) - y;
+          lo_s = t;
         }
       });
-      // each thread's float sum to fixed point, then exact integer sums; the error bound covers the
-      // compensated sums' rounding (a few ulps of each thread's sum), the conversions, and each of the
-      // <= V weights the exact sum truncates
-      const unsigned long long te = block_sum_u64(fixed40(tot.s + tot.c), wsum);
-      const unsigned long long ae = block_sum_u64(fixed40(above.s + above.c), wsum);
-      const unsigned long long slack = static_cast<unsigned long long>(V) + 2 * kTT;
-      const unsigned long long terr = (te >> 20) + slack, aerr = (ae >> 20) + slack;
+      // each thread's float sums to fixed point, then exact integer sums.  Error bounds (relative): 2^-21
+      // for the compensated sum; (n - 1) 2^-24 for a plain sum of n positive terms, n the largest count
+      // of any thread; plus the conversions (one unit per thread and sum) and the <= V weights the exact
+      // sum truncates.
+      const unsigned long long le = block_sum_u64(fixed40(lo_s - lo_c), wsum);
+      const unsigned long long ie = block_sum_u64(fixed40(tin), wsum);
+      const unsigned long long ae = block_sum_u64(fixed40(tab), wsum);
+      const double nmax = block_max_u32(max(nin, nab), wsum);
+      const unsigned long long te = le + ie + ae;
+      const double u = 5.9604644775390625e-8 * 1.01;
+      const unsigned long long slack = static_cast<unsigned long long>(V) + 4 * kTT;
+      const unsigned long long aerr = static_cast<unsigned long long>(static_cast<double>(ae) * nmax * u) + slack;
+      const unsigned long long terr = static_cast<unsigned long long>(static_cast<double>(le) * 4.76837158203125e-7 +
+                                                                      static_cast<double>(ie + ae) * nmax * u) +
+                                      slack;
       const unsigned long long nlo = nucleus_need(top_p, O + (te > terr ? te - terr : 0ull));
       const unsigned long long nhi = nucleus_need(top_p, O + te + terr);
       const int n = cnt;
       if (n <= kCap) {
-        int n2 = 1;
-        while (n2 < n) n2 <<= 1;
-        for (int i = n + tid; i < n2; i += kTT) cand[i] = -INFINITY;
-        __syncthreads();
-        sort_desc(cand, n2);
-        unsigned long long local = 0;
-        for (int i = tid; i < n; i += kTT) local += weight(cand[i]);
-        const unsigned long long ct = block_sum_u64(local, wsum);
+        // the candidates largest first: ranked in place of a sort when at most kTT
+        float* sc = cand;
+        if (n <= kTT) {
+          sc = cand + kCap / 2;
+          rank_sort(cand, n, sc);
+        } else {
+          int n2 = 1;
+          while (n2 < n) n2 <<= 1;
+          for (int i = n + tid; i < n2; i += kTT) cand[i] = -INFINITY;
+          __syncthreads();
+          sort_desc(cand, n2);
+        }
         const unsigned long long alo = ae > aerr ? ae - aerr : 0ull, ahi = ae + aerr;
         if (nhi <= O) {  // inside the overflow, whatever the exact total
-          const int i0 = first_reaching<kOver / kTT>(over, no, nlo, units, wsum, &sel);
-          const int i1 = first_reaching<kOver / kTT>(over, no, nhi, units, wsum, &sel);
-          if (over[i0] == over[i1]) {
-            if (tid == 0) thr[blockIdx.x] = over[i0];
+          const Reach r = reach_two<kOver / kTT>(over, no, nlo, nhi, units, wsum, &rc);
+          if (over[r.a] == over[r.b]) {
+            if (tid == 0) thr[blockIdx.x] = over[r.a];
             return;
           }
-        } else if (nlo > O + ahi && nhi - O - alo <= ct) {  // inside the candidates, whatever the exact sums
-          const int i0 = first_reaching<kCap / kTT>(cand, n, nlo - O - ahi, units, wsum, &sel);
-          const int i1 = first_reaching<kCap / kTT>(cand, n, nhi - O - alo, units, wsum, &sel);
-          if (cand[i0] == cand[i1]) {
-            if (tid == 0) thr[blockIdx.x] = cand[i0];
+        } else if (nlo > O + ahi) {  // past the logits above the interval, whatever the exact sums
+          const Reach r = reach_two<kCap / kTT>(sc, n, nlo - O - ahi, nhi - O - alo, units, wsum, &rc);
+          if (r.a >= 0 && r.b >= 0 && sc[r.a] == sc[r.b]) {
+            if (tid == 0) thr[blockIdx.x] = sc[r.a];
             return;
           }
         }
@@ -682,10 +778,12 @@ __global__ void __launch_bounds__(kTT, 3) threshold_kernel(const void* __restric
           if (tid == 0) thr[blockIdx.x] = over[i];
           return;
         }
-        if (need > O + ax && need - O - ax <= ct) {
-          const int i = first_reaching<kCap / kTT>(cand, n, need - O - ax, units, wsum, &sel);
-          if (tid == 0) thr[blockIdx.x] = cand[i];
-          return;
+        if (need > O + ax) {
+          const Reach r = reach_two<kCap / kTT>(sc, n, need - O - ax, need - O - ax, units, wsum, &rc);
+          if (r.a >= 0) {
+            if (tid == 0) thr[blockIdx.x] = sc[r.a];
+            return;
+          }
         }
       }
       // more logits in the interval than the buffer holds, or a threshold outside it (not expected):
@@ -716,6 +814,18 @@ __global__ void __launch_bounds__(kTT, 3) threshold_kernel(const void* __restric
     }
   }
   const int n = cnt;
+  if (!kTopP && n <= kTT) {  // the need2-th largest by rank, no sort
+    if (tid < n) {
+      const float f = cand[tid];
+      int r = 0;
+      for (int j = 0; j < n; ++j) {
+        const float g = cand[j];
+        r += (g > f || (g == f && j < tid)) ? 1 : 0;
+      }
+      if (r == static_cast<int>(need2) - 1) thr[blockIdx.x] = f;
+    }
+    return;
+  }
   if (n > kCap) {  // too many to sort here: exact radix selection over the bin
     const uint32_t key = radix_select<T, kTopP>(row, V, vv, R, b48, db, need2, masses, wsum, &pk, weight);
     if (tid == 0) thr[blockIdx.x] = key_float(key);
