@@ -50,8 +50,12 @@ struct DrawSmem {
   float2 cs[kMaxRowChunks];  // chunk masses of the drawn row (w, p), gathered by the resolving CTA
   float2 ds[kMaxSlices];     // slice masses of the drawn row (w, p)
   uint32_t err;
-  int last, pick, mode;
+  int last, pick, mode, c0, c1;
   float t, pre;
+  // a draw from p over several stream slices: the chunks [pcl, pch) of the slice the partials place u_final
+  // in and the mass to find inside it (pcl = -1: the whole row's chunks)
+  int pcl, pch;
+  float ptp;
 };
 
 // Inputs of the row's decisions that the stream kernel does not write, loaded by the draw kernel before
@@ -68,6 +72,44 @@ __device__ __forceinline__ RowInputs load_row_inputs(const SampleParams& a, int 
   if (tid < gb) in.u = __ldg(a.uniforms + (size_t)b * (a.G + 1) + tid);
   if (tid == 0) in.uf = __ldg(a.uniforms + (size_t)b * (a.G + 1) + a.G);
   return in;
+}
+
+// A draw from p_n over a row of NS > 1 stream slices, by warp 0: the slice masses p(slice s) =
+// S_s 2^((m_s - M) log2(e)/T) / S from the stream pass's partials of position n, summed in the order that
+// made S (so that they total exactly 1); the slice holding u_final -- the first of positive mass whose
+// running total passes it -- into sm as its chunk range [pcl, pch) (cpc elements per chunk; stream slices
+// are whole chunks), with the mass u_final - (the slices before it) left to find inside it (pcl = -1 if
+// no slice has mass).  uf is read from lane 0.  Only the chosen slice's chunks are then read again.
+__device__ __noinline__ void partial_pick(const SampleParams& a, int b, int n, float uf, int cpc, DrawSmem& sm) {
+  const int lane = threadIdx.x & 31;
+  const int NS = a.nslices;
+  const float4 pr = load_partial(reinterpret_cast<const float4*>(a.ws.part) + ((size_t)b * (a.G + 1) + n) * NS, NS);
+  const float M = sm.mp[n], S = sm.sp[n];
+  // the same terms, summed in the same order, as combine_partials
+  const float P = (pr.x > -INFINITY && M < INFINITY) ? pr.y * fast_exp2((pr.x - M) * a.scale) : 0.f;
+  float pre = 0.f, run = 0.f;
+  for (int r = 0; r < NS; ++r) {
+    if (r == lane) pre = run;
+    run += __shfl_sync(0xffffffffu, P, r);
+  }
+  const float u = __shfl_sync(0xffffffffu, uf, 0);
+  const float cum = (pre + P) / S;  // pre + P: the running sum after this slice, the float combine saw
+  // u < 1 and the last slice of positive mass ends at S / S = 1, so a slice of positive mass is found
+  const unsigned hit = __ballot_sync(0xffffffffu, lane < NS && P > 0.f && cum > u);
+  const unsigned pos = __ballot_sync(0xffffffffu, lane < NS && P > 0.f);
+  const int sl = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
+  const float pre_s = __shfl_sync(0xffffffffu, pre, sl < 0 ? 0 : sl);
+  if (lane == 0) {
+    if (sl < 0) {
+      sm.pcl = -1;
+    } else {
+      const int per = a.slice / cpc;
+      const int nc = (a.V + cpc - 1) / cpc;
+      sm.pcl = sl * per;
+      sm.pch = min(sl * per + per, nc);
+      sm.ptp = fmaxf(u - pre_s / S, 0.f);
+    }
+  }
 }
 
 // staged: the caller already put the row normalisers in sm.mp .. sm.sq and the logits at the draft
@@ -190,7 +232,9 @@ __device__ __forceinline__ void slice_sums(DrawSmem& sm, int ND, int cps, int nc
 }
 
 // Last CTA of row b: slice, chunk and token of the draw; the row's outputs; every slot back to zero.
-template <typename T>
+// kPick: the row has several stream slices, and a draw from p may take its slice from the partials
+// (partial_pick); without it every draw scans the whole row's chunks.
+template <typename T, bool kPick>
 __device__ void resolve_row(const SampleParams& a, int b, int gb, const RowState& st, DrawSmem& sm) {
   constexpr int kV = Elems<T>::kVec;
   const int tid = threadIdx.x, lane = tid & 31;
@@ -204,6 +248,8 @@ __device__ void resolve_row(const SampleParams& a, int b, int gb, const RowState
   int32_t* e = a.emitted + (size_t)b * G1;
   const bool resid = st.flags & kRowResid;
   const bool failed = st.flags & kRowInvalid;
+  // a draw from p whose stream slice the partials picked (sm.pcl >= 0): only that slice's chunks count
+  bool pmode = kPick && !failed && sm.pcl >= 0;
   // the chunk masses of the whole row in shared memory: already there when the row has one draw CTA,
   // else one round trip for all of them
   const bool staged = ND == 1 || a.cluster != 0;
@@ -211,18 +257,29 @@ __device__ void resolve_row(const SampleParams& a, int b, int gb, const RowState
     for (int c = tid; c < ND * cps; c += kST) sm.cs[c] = __ldcg(dch + c);
   __syncthreads();
   // slice masses: one warp per slice, a fixed-order reduction of its chunk masses
-  if (!failed) slice_sums(sm, ND, cps, nc, 3);
+  if (!failed && !pmode) slice_sums(sm, ND, cps, nc, 3);
   __syncthreads();
   if (!failed && resid) {
     // a residual whose mass is degenerate (<= 1e-15) draws from p instead; the draw CTAs summed only the
-    // residual, so this CTA sums the p masses of the row's chunks now (rare: a rejection implies a
-    // positive residual in exact arithmetic)
+    // residual, so this CTA sums the p masses of the chunks now -- of the slice the partials pick when the
+    // row has several stream slices, else of the whole row (rare: a rejection implies a positive residual
+    // in exact arithmetic)
     float Z = 0.f;
     for (int d = 0; d < ND; ++d) Z += sm.ds[d].x;
     if (!(Z > kZFloor)) {
       const int warp = tid >> 5;
       const T* tr = reinterpret_cast<const T*>(a.target) + ((size_t)b * G1 + st.n) * a.V;
-      for (int c = warp; c < nc; c += kSW) {
+      int pc0 = 0, pc1 = nc;
+      if (kPick) {
+        if (tid < 32) partial_pick(a, b, st.n, st.uf, cpc, sm);
+        __syncthreads();
+        pmode = sm.pcl >= 0;
+        if (pmode) {
+          pc0 = sm.pcl;
+          pc1 = sm.pch;
+        }
+      }
+      for (int c = pc0 + warp; c < pc1; c += kSW) {
         float lp = 0.f;
 #pragma unroll
         for (int r = 0; r < kR; ++r) {
@@ -234,11 +291,21 @@ __device__ void resolve_row(const SampleParams& a, int b, int gb, const RowState
         if (lane == 0) sm.cs[c].y = lp;
       }
       __syncthreads();
-      slice_sums(sm, ND, cps, nc, 2);
-      __syncthreads();
+      if (!pmode) {
+        slice_sums(sm, ND, cps, nc, 2);
+        __syncthreads();
+      }
     }
   }
-  if (!failed && tid == 0) {
+  if (pmode && tid == 0) {  // the chunks of the partials' slice, the target mass inside it
+    sm.c0 = sm.pcl;
+    sm.c1 = sm.pch;
+    sm.t = sm.ptp;
+    sm.pre = 0.f;
+    sm.mode = 1;
+    sm.pick = 0;
+  }
+  if (!failed && !pmode && tid == 0) {
     // total mass in slice order; the residual, or p when the residual mass is degenerate
     const float uf = st.uf;
     float Z = 0.f, P = 0.f;
@@ -272,6 +339,8 @@ __device__ void resolve_row(const SampleParams& a, int b, int gb, const RowState
     sm.mode = (use_p ? 1 : 0) | (fallback ? 2 : 0);
     sm.t = t;
     sm.pre = pre;
+    sm.c0 = sd * cps;
+    sm.c1 = min(sd * cps + cps, nc);
   }
   if (failed && tid == 0) sm.pick = -1;
   __syncthreads();
@@ -281,11 +350,11 @@ __device__ void resolve_row(const SampleParams& a, int b, int gb, const RowState
   const int sd = sm.pick;
   if (sd >= 0) {
     if (tid < 32) {
-      const int c0 = sd * cps, c1 = min(c0 + cps, nc);
+      const int c0 = sm.c0, c1 = sm.c1;
       const bool use_p = sm.mode & 1;
       const bool fb = sm.mode & 2;
       const float t = sm.t;
-      const int m = (cps + 31) / 32;
+      const int m = (c1 - c0 + 31) / 32;
       const int r0 = c0 + lane * m, r1 = min(r0 + m, c1);
       float ls = 0.f;
       int lpos = -1;
@@ -511,7 +580,7 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_stream_kernel(const 
 
 // Draw slice d of batch row b once the row's slice normalisers are in the workspace: decisions, chunk
 // masses of the drawn row(s) in this slice, and the row's resolution in its last draw CTA.
-template <typename T>
+template <typename T, bool kPick>
 __device__ __forceinline__ void draw_slice_of_row(const SampleParams& a, int b, int d, int gb, const RowInputs& in,
                                                   DrawSmem& sm, bool staged = false) {
   constexpr int kV = Elems<T>::kVec;
@@ -528,6 +597,15 @@ __device__ __forceinline__ void draw_slice_of_row(const SampleParams& a, int b, 
     return;
   }
   const RowState st = decide_row(a, b, gb, in, sm, staged);
+  // a draw from p over several stream slices: only the slice the partials place u_final in is read again
+  if (kPick) {
+    if (tid == 0) sm.pcl = -1;
+    __syncthreads();
+    if (!(st.flags & (kRowInvalid | kRowResid))) {
+      if (tid < 32) partial_pick(a, b, st.n, in.uf, kR * 32 * kV, sm);
+      __syncthreads();
+    }
+  }
   // a clustered row (a.cluster): every CTA stores its chunk masses straight into the shared memory of
   // rank 0, which resolves the row; every CTA has started once the start-of-kernel arrivals are met
   const bool clustered = a.cluster != 0;
@@ -544,8 +622,12 @@ __device__ __forceinline__ void draw_slice_of_row(const SampleParams& a, int b, 
     const int seg = 32 * kV;                     // elements per segment
     const int cpc = kR * seg;                    // elements per chunk
     const int cps = a.dslice / cpc;              // chunks per slice
-    const int c0 = d * cps;
-    const int c1 = min(c0 + cps, (a.V + cpc - 1) / cpc);
+    int c0 = d * cps;
+    int c1 = min(c0 + cps, (a.V + cpc - 1) / cpc);
+    if (kPick && sm.pcl >= 0) {
+      c0 = max(c0, sm.pcl);
+      c1 = min(c1, sm.pch);
+    }
     float2* dch = reinterpret_cast<float2*>(a.ws.dch) + (size_t)b * ND * cps;
     if (!bounds_ok(cps <= kMaxChunksPerSlice && ND * cps <= kMaxRowChunks &&
                        (size_t)ND * cps <= chunks_per_row(a.V) && st.n <= gb,
@@ -553,7 +635,7 @@ __device__ __forceinline__ void draw_slice_of_row(const SampleParams& a, int b, 
       return;
     const float sc = a.scale;
     for (int c = c0 + warp; c < c1; c += kSW) {
-      float lw = 0.f, lp = 0.f;
+      float lw = 0.f;
       if (vec && (c + 1) * cpc <= a.V) {
         uint4 rt[kR], rd[kR];
 #pragma unroll
@@ -626,7 +708,7 @@ __device__ __forceinline__ void draw_slice_of_row(const SampleParams& a, int b, 
   }
   if (clustered) {
     cluster_sync();  // every CTA's chunk masses are in rank 0's shared memory
-    if (cluster_ctarank() == 0) resolve_row<T>(a, b, gb, st, sm);
+    if (cluster_ctarank() == 0) resolve_row<T, kPick>(a, b, gb, st, sm);
     return;
   }
   __syncthreads();  // every warp's chunk masses written (and fenced) before the arrival
@@ -641,11 +723,11 @@ __device__ __forceinline__ void draw_slice_of_row(const SampleParams& a, int b, 
   __syncthreads();
   if (sm.last) {
     if (ND > 1) __threadfence();
-    resolve_row<T>(a, b, gb, st, sm);
+    resolve_row<T, kPick>(a, b, gb, st, sm);
   }
 }
 
-template <typename T>
+template <typename T, bool kPick>
 __global__ void __launch_bounds__(kStreamThreads, 4) verify_draw_kernel(const SampleParams a) {
   __shared__ DrawSmem sm;
   if (a.cluster) cluster_arrive_relaxed();  // this CTA has started (its shared memory may be written)
@@ -659,7 +741,7 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_draw_kernel(const Sa
   const RowInputs in = (gb >= 0 && gb <= a.G) ? load_row_inputs(a, b, gb) : RowInputs{0, 0.f, 0.f};
   // launched as a programmatic dependent of the stream kernel: wait for all of it (and its writes)
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  draw_slice_of_row<T>(a, b, d, gb, in, sm);
+  draw_slice_of_row<T, kPick>(a, b, d, gb, in, sm);
 }
 
 // ----------------------------------------------------------------------------- short rows, one launch
@@ -747,7 +829,7 @@ __global__ void __launch_bounds__(kStreamThreads, 4) verify_short_kernel(const S
     }
   }
   __syncthreads();  // the normalisers in shared memory
-  draw_slice_of_row<T>(a, b, 0, gb, in, sm, true);
+  draw_slice_of_row<T, false>(a, b, 0, gb, in, sm, true);
 }
 
 // The one-launch path applies to 16-byte aligned rows of at most kShortRowBytes with one stream slice and
@@ -803,7 +885,8 @@ static cudaError_t launch_draw(const SampleParams& p, cudaStream_t stream) {
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = q.cluster ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, verify_draw_kernel<T>, q);
+  return p.nslices > 1 ? cudaLaunchKernelEx(&cfg, verify_draw_kernel<T, true>, q)
+                       : cudaLaunchKernelEx(&cfg, verify_draw_kernel<T, false>, q);
 }
 
 // The early exit runs the one-launch kernel, which streams a row's positions one after the other and
