@@ -21,14 +21,17 @@
 //   first rejection n -- the same arithmetic in every CTA, so they agree bit
 //   for bit -- then, over slice d of target row n (and of draft row n for a
 //   residual draw), writes the mass of w = max(0, p_n - q_n) and of p_n per
-//   chunk.  The last CTA of row b (atomic arrival counter) picks, from
+//   chunk.  A draw from p_n over a row of several stream slices takes its
+//   slice from the stream pass's slice normalisers first, and only that
+//   slice's chunks are summed.  The last CTA of row b (atomic arrival counter) picks, from
 //   u_final * (total mass), the slice, then the chunk from the stored chunk
 //   masses, then the token by warp scans over that chunk's recomputed
 //   weights: the residual draw, the draw from p_n when the residual mass is
 //   <= 1e-15, or the bonus draw from p_{gamma_b} when nothing was rejected.
 //   It writes the row's outputs and returns every slot the row used to zero.
 // p and q are never written to memory; HBM traffic is the logits read once
-// plus at most the two drawn rows per batch row that have left L2.
+// plus, per batch row, at most the two drawn rows (a residual draw) or one
+// stream slice of the drawn row (a draw from p), where they have left L2.
 #include <cstdlib>
 
 #include "common.cuh"
