@@ -43,7 +43,9 @@
  *    SPECVERIFY_CLUSTER / SPECVERIFY_STATS_SLICE (statistics cluster size /
  *    slice), SPECVERIFY_DRAW_CLUSTER (0 / 1: a row's draw CTAs as a
  *    thread-block cluster), SPECVERIFY_PDL=0 (plain launch of a call's first
- *    kernel).
+ *    kernel), SPECVERIFY_NUCLEUS_PATH=bounds / exact / weighted (how the
+ *    nucleus threshold of a row over 128 KB is selected; the same threshold
+ *    either way).
  *  - A row is invalid if any logit row it reads holds a NaN or +inf or is
  *    entirely -inf.  Ragged rows (draft_len[b] = gamma_b < gamma) never read
  *    target rows i > gamma_b, draft rows i >= gamma_b, ids i >= gamma_b, or

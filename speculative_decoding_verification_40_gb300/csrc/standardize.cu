@@ -33,6 +33,9 @@
 // each).
 #include <cuda_bf16.h>
 
+#include <cstdlib>
+#include <cstring>
+
 #include "../../include/spec_verify.h"
 #include "common.cuh"
 #include "softmax.cuh"
@@ -565,7 +568,7 @@ __device__ Bracket nucleus_bracket(const Hist& h, unsigned long long base, float
 // pass 1 is run again against R = M, where nothing lies above the reference.
 template <typename T, bool kTopP, bool kWhole>
 __global__ void __launch_bounds__(kTT, 3) threshold_kernel(const void* __restrict__ logits, int V, int k, float scale,
-                                                           float top_p, int vec, float* __restrict__ thr) {
+                                                           float top_p, int vec, int path, float* __restrict__ thr) {
   // the histogram and the gathered logits share one buffer: the logits are gathered after the histogram
   // is read
   __shared__ __align__(16) unsigned char buf[kBufBytes];
@@ -684,7 +687,7 @@ __global__ void __launch_bounds__(kTT, 3) threshold_kernel(const void* __restric
   } else {
     bool weighted = true;
     const Bracket br = whole ? Bracket{0, 0, ~0ull} : nucleus_bracket(counts, O, top_p, wsum, wsum2, &bk);
-    if (!whole && br.count <= static_cast<unsigned long long>(kCap)) {
+    if (!whole && path != 2 && br.count <= static_cast<unsigned long long>(kCap)) {
       // a logit interval holding the bracket's bins: dist_bin(l) in [first, last] gives x_lo <= l <= x_hi,
       // half a bin of margin at each end for the bins' rounding
       const float x_hi = R - (static_cast<float>(br.first) - 0.5f) / b48;
@@ -748,7 +751,9 @@ __global__ void __launch_bounds__(kTT, 3) threshold_kernel(const void* __restric
           sort_desc(cand, n2);
         }
         const unsigned long long alo = ae > aerr ? ae - aerr : 0ull, ahi = ae + aerr;
-        if (nhi <= O) {  // inside the overflow, whatever the exact total
+        if (path == 1) {
+          // the exact pass below, whatever the bounds say
+        } else if (nhi <= O) {  // inside the overflow, whatever the exact total
           const Reach r = reach_two<kOver / kTT>(over, no, nlo, nhi, units, wsum, &rc);
           if (over[r.a] == over[r.b]) {
             if (tid == 0) thr[blockIdx.x] = over[r.a];
@@ -844,14 +849,26 @@ __global__ void __launch_bounds__(kTT, 3) threshold_kernel(const void* __restric
 
 namespace {
 
+// The nucleus selection of long rows: 0 = the float sums' bounds decide, the exact pass only where they
+// leave two candidates; 1 = always the exact pass; 2 = always the weighted histogram.  All three give the
+// same thresholds; SPECVERIFY_NUCLEUS_PATH=bounds / exact / weighted picks one (for tests).
+int nucleus_path() {
+  const char* env = std::getenv("SPECVERIFY_NUCLEUS_PATH");
+  if (!env) return 0;
+  if (std::strcmp(env, "exact") == 0) return 1;
+  if (std::strcmp(env, "weighted") == 0) return 2;
+  return 0;
+}
+
 // Rows of at most kSampleRowBytes take the kernel that reads the whole row for R (the exact max).
 template <typename T, bool kTopP>
 cudaError_t threshold_launch(const void* logits, int R, int V, int k, float scale, float top_p, int vec, float* thr,
                              cudaStream_t stream) {
+  const int path = kTopP ? nucleus_path() : 0;
   if (static_cast<long long>(V) * sizeof(T) <= kSampleRowBytes)
-    threshold_kernel<T, kTopP, true><<<R, kTT, 0, stream>>>(logits, V, k, scale, top_p, vec, thr);
+    threshold_kernel<T, kTopP, true><<<R, kTT, 0, stream>>>(logits, V, k, scale, top_p, vec, path, thr);
   else
-    threshold_kernel<T, kTopP, false><<<R, kTT, 0, stream>>>(logits, V, k, scale, top_p, vec, thr);
+    threshold_kernel<T, kTopP, false><<<R, kTT, 0, stream>>>(logits, V, k, scale, top_p, vec, path, thr);
   return cudaGetLastError();
 }
 

@@ -111,6 +111,30 @@ def test_thresholds_on_every_selection_path(S, V, dtype, offset):
                 assert np.float32(thr[r]) == np.float32(tau), (top_p, r, thr[r], tau)
 
 
+@pytest.mark.parametrize("V,dtype", [(152064, "f32"), (128256, "bf16"), (200003, "f32")])
+def test_nucleus_selection_paths_agree(S, monkeypatch, V, dtype):
+    """Rows over 128 KB select the nucleus threshold from float sums whose error bounds must leave a single
+    candidate, else from an exact fixed-point pass; a bracket too wide takes the weighted histogram.  The
+    three (SPECVERIFY_NUCLEUS_PATH = bounds / exact / weighted) must give the same bits, and match the
+    oracle outside flagged rows.  V = 200003 fp32 rows are not 16-byte aligned (scalar loads)."""
+    R = 16
+    l = _random_rows(R, V, dtype, 91, 0)
+    l = (l.float() + W.zipf_log_prior(V, 1.0, "cuda")[None, :]).to(l.dtype)
+    h, dt = _rows_np(l)
+    for top_p, T in ((0.5, 1.0), (0.9, 0.7), (0.99, 1.3)):
+        outs = []
+        for path in ("bounds", "exact", "weighted"):
+            monkeypatch.setenv("SPECVERIFY_NUCLEUS_PATH", path)
+            outs.append(S.topp_threshold(l, T, top_p).view(torch.int32).cpu())
+        monkeypatch.delenv("SPECVERIFY_NUCLEUS_PATH")
+        assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2]), (top_p, outs)
+        thr = outs[0].view(torch.float32).numpy()
+        for r in range(R):
+            tau, flag = O.topp_threshold(O.widen(h[r], dt), float(np.float32(T)), float(np.float32(top_p)))
+            if not flag:
+                assert np.float32(thr[r]) == np.float32(tau), (top_p, r, thr[r], tau)
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("top_p,T", [(0.5, 1.0), (0.9, 0.7), (0.99, 1.3), (0.05, 1.0), (1.0, 1.0)])
 def test_topp_threshold_matches_oracle(S, dtype, top_p, T):
