@@ -556,8 +556,7 @@ __device__ Bracket nucleus_bracket(const Hist& h, unsigned long long base, float
 //     gathered (or, past kCap logits, the radix selection) gives the threshold.
 //   nucleus: a bin's count bounds its mass within about 1.6 %, so the counts bracket the bins the running
 //     mass top_p * total can end in; pass 2 gathers the logits of a logit interval holding those bins and
-//     sums every weight in float (compensated for the many below the interval): the total, and the mass
-//     above the interval.  The candidates' exact fixed-point weights are then scanned, in descending
+//     sums every weight in float: the total, and the mass above the interval.  The candidates' exact fixed-point weights are then scanned, in descending
 //     order, for the running mass top_p * total taken at both ends of the sums' error bounds: if both ends
 //     stop at the same logit, that logit is the threshold the exact fixed-point sums give; otherwise
 //     (rare: 1 or 2 of 1536 c3 rows) a pass of exact fixed-point sums decides.  A bracket of more than
@@ -693,10 +692,9 @@ __global__ void __launch_bounds__(kTT, 3) threshold_kernel(const void* __restric
       const float x_hi = R - (static_cast<float>(br.first) - 0.5f) / b48;
       const float x_lo = R - (static_cast<float>(br.last) + 1.5f) / b48;
       // pass 2: the interval's logits into shared memory, and every weight summed in float: below the
-      // interval (the common case: one comparison, a compensated sum), inside it, and above it up to R
-      // (plain sums, with their term counts; the logits above R are the overflow, whose exact mass is O;
-      // -inf weighs 0)
-      float lo_s = 0.f, lo_c = 0.f, tin = 0.f, tab = 0.f;
+      // interval (the common case: one comparison and one add), inside it, and above it up to R (with
+      // their term counts; the logits above R are the overflow, whose exact mass is O; -inf weighs 0)
+      float tlow = 0.f, tin = 0.f, tab = 0.f;
       unsigned int nin = 0, nab = 0;
       for_each_logit<T>(row, V, vv, [&](float f) {
         const float w = fast_exp2(fmaf(f, scale, nm));
@@ -712,18 +710,16 @@ __global__ void __launch_bounds__(kTT, 3) threshold_kernel(const void* __restric
               if (at < kCap) cand[at] = f;
             }
           }
-        } else {  // Kahan: lo_s + lo_c holds the sum to within a few ulps of it
-          const float y = w - lo_c;
-          const float t = lo_s + y;
-          lo_c = (t - lo_s) - y;
-          lo_s = t;
+        } else {
+          tlow += w;
         }
       });
-      // each thread's float sums to fixed point, then exact integer sums.  Error bounds (relative): 2^-21
-      // for the compensated sum; (n - 1) 2^-24 for a plain sum of n positive terms, n the largest count
-      // of any thread; plus the conversions (one unit per thread and sum) and the <= V weights the exact
-      // sum truncates.
-      const unsigned long long le = block_sum_u64(fixed40(lo_s - lo_c), wsum);
+      // each thread's float sums to fixed point, then exact integer sums.  A float sum of n positive terms
+      // is within (n - 1) 2^-24 of its exact value (relative): n is at most V / kTT + 64 for the sum below
+      // the interval (the mass beyond the nucleus, a small part of the total for the usual top_p) and the
+      // largest count of any thread for the other two; plus the conversions (one unit per thread and sum)
+      // and the <= V weights the exact sum truncates.
+      const unsigned long long le = block_sum_u64(fixed40(tlow), wsum);
       const unsigned long long ie = block_sum_u64(fixed40(tin), wsum);
       const unsigned long long ae = block_sum_u64(fixed40(tab), wsum);
       const double nmax = block_max_u32(max(nin, nab), wsum);
@@ -731,9 +727,10 @@ __global__ void __launch_bounds__(kTT, 3) threshold_kernel(const void* __restric
       const double u = 5.9604644775390625e-8 * 1.01;
       const unsigned long long slack = static_cast<unsigned long long>(V) + 4 * kTT;
       const unsigned long long aerr = static_cast<unsigned long long>(static_cast<double>(ae) * nmax * u) + slack;
-      const unsigned long long terr = static_cast<unsigned long long>(static_cast<double>(le) * 4.76837158203125e-7 +
-                                                                      static_cast<double>(ie + ae) * nmax * u) +
-                                      slack;
+      const double nlow = static_cast<double>(V) / kTT + 64.0;
+      const unsigned long long terr =
+          static_cast<unsigned long long>(static_cast<double>(le) * nlow * u + static_cast<double>(ie + ae) * nmax * u) +
+          slack;
       const unsigned long long nlo = nucleus_need(top_p, O + (te > terr ? te - terr : 0ull));
       const unsigned long long nhi = nucleus_need(top_p, O + te + terr);
       const int n = cnt;
