@@ -408,7 +408,9 @@ __device__ Reach reach_two(const float* s, int n, unsigned long long need_a, uns
 // are appended to over[] (*nover counts them all, and may pass kOver), their max is returned in *omax, and
 // whether a NaN or +inf was seen is returned, block-wide; the common case, a finite logit at or below R,
 // takes one comparison before its bin.  Without kAbove R is the row max and the row holds no NaN or +inf.
-template <typename T, bool kAbove>
+// A -inf logit lands in the far bin (the fminf in dist_bin), which counts only finite logits -- unless
+// kNoFar: the far bin's count is not used (the nucleus: its weights truncate to 0), and counts -inf too.
+template <typename T, bool kAbove, bool kNoFar>
 __device__ bool count_pass(const T* row, int V, bool vv, float R, float s48, const Hist& hist, float* over,
                            int* nover, unsigned long long* wsum, float* red, float* omax) {
   hist.zero(kBins);
@@ -424,10 +426,10 @@ __device__ bool count_pass(const T* row, int V, bool vv, float R, float s48, con
       } else {  // NaN or +inf
         bad = 1;
       }
-    } else if (f > -INFINITY) {
+    } else {
       const int bin = dist_bin(f, R, s48);
       if (bin == kBins - 1)
-        ++tail;
+        tail += (kNoFar || f > -INFINITY) ? 1u : 0u;
       else
         atomicAdd(hist.lo + (kBins - 1 - bin), 1u);
     }
@@ -622,7 +624,7 @@ __global__ void __launch_bounds__(kTT, 3) threshold_kernel(const void* __restric
 
   // pass 1: counts per distance bin against R, the overflow and its max
   float omax = -INFINITY;
-  if (!(kTopP && whole) && count_pass<T, !kWhole>(row, V, vv, R, b48, counts, over, &nover, wsum, red, &omax)) {
+  if (!(kTopP && whole) && count_pass<T, !kWhole, kTopP>(row, V, vv, R, b48, counts, over, &nover, wsum, red, &omax)) {
     if (tid == 0) thr[blockIdx.x] = NAN;  // NaN or +inf in the row
     return;
   }
@@ -640,7 +642,7 @@ __global__ void __launch_bounds__(kTT, 3) threshold_kernel(const void* __restric
     // pass 1 again against the true max: no logit lies above it (nover is left as it is)
     R = M;
     nm = -R * scale;
-    count_pass<T, !kWhole>(row, V, vv, R, b48, counts, over, &nover, wsum, red, &omax);
+    count_pass<T, !kWhole, kTopP>(row, V, vv, R, b48, counts, over, &nover, wsum, red, &omax);
     no = 0;
   }
 
