@@ -677,9 +677,12 @@ __global__ void __launch_bounds__(kTT, 3) threshold_kernel(const void* __restric
     const Pick p = pick_from_top(counts, kBins, static_cast<unsigned long long>(k) - O, wsum, &pk);
     db = kBins - 1 - p.bin;
     need2 = static_cast<unsigned long long>(k) - O - p.above;
-    // pass 2: the bin's logits into shared memory
+    // pass 2: the bin's logits into shared memory.  dist_bin(l) = db gives x_lo <= l (half a bin of margin
+    // for the bin's rounding), so one comparison passes over every other logit; the few at or above x_lo
+    // take the exact test
+    const float x_lo = db < kBins - 1 ? R - (static_cast<float>(db) + 1.5f) / b48 : -INFINITY;
     for_each_logit<T>(row, V, vv, [&](float f) {
-      if (f <= R && f > -INFINITY && dist_bin(f, R, b48) == db) {
+      if (f >= x_lo && f <= R && f > -INFINITY && dist_bin(f, R, b48) == db) {
         const int at = atomicAdd(&cnt, 1);
         if (at < kCap) cand[at] = f;
       }
