@@ -340,21 +340,46 @@ __device__ int first_reaching(const float* s, int n, unsigned long long need, U&
   return r;
 }
 
-// Descending order of n <= kTT gathered logits without a sorting network: thread t counts the logits that
-// come before cand[t] (larger, or equal with a smaller index) and stores cand[t] at that position of out.
-// One barrier.
-__device__ __forceinline__ void rank_sort(const float* cand, int n, float* out) {
+// Among n <= kTT gathered logits (in any order): the logit at which the running sum of units, taken from the
+// largest down (ties by index), first reaches need_a, and the one for need_b.  Thread t sums the units
+// of the logits that come before cand[t] in that order, so no sort or scan is needed; w holds the units
+// (kTT slots).  found[k] = 0 if the whole sum stays below the need.  Every thread gets the results.
+struct Reached {
+  float a, b;
+  int found_a, found_b;
+};
+
+template <typename U>
+__device__ Reached reach_small(const float* cand, int n, unsigned long long need_a, unsigned long long need_b,
+                               U&& units, unsigned long long* w, Reached* out) {
   const int t = threadIdx.x;
+  if (t == 0) {
+    out->found_a = 0;
+    out->found_b = 0;
+  }
+  if (t < n) w[t] = units(cand[t]);
+  __syncthreads();
   if (t < n) {
     const float f = cand[t];
-    int r = 0;
+    unsigned long long pre = 0;
     for (int j = 0; j < n; ++j) {
       const float g = cand[j];
-      r += (g > f || (g == f && j < t)) ? 1 : 0;
+      if (g > f || (g == f && j < t)) pre += w[j];
     }
-    out[r] = f;
+    const unsigned long long post = pre + w[t];
+    if (pre < need_a && need_a <= post) {
+      out->a = f;
+      out->found_a = 1;
+    }
+    if (pre < need_b && need_b <= post) {
+      out->b = f;
+      out->found_b = 1;
+    }
   }
   __syncthreads();
+  const Reached r = *out;
+  __syncthreads();
+  return r;
 }
 
 // Over s[0, n) (n <= kPer * kTT, largest first) with units(s[i]): the first index whose running sum reaches
@@ -583,6 +608,7 @@ __global__ void __launch_bounds__(kTT, 3) threshold_kernel(const void* __restric
   __shared__ Pick pk;
   __shared__ Bracket bk;
   __shared__ Reach rc;
+  __shared__ Reached rs;
   __shared__ int cnt, nover, sel;
   const int tid = threadIdx.x;
   const T* row = reinterpret_cast<const T*>(logits) + (size_t)blockIdx.x * V;
@@ -740,12 +766,10 @@ __global__ void __launch_bounds__(kTT, 3) threshold_kernel(const void* __restric
       const unsigned long long nhi = nucleus_need(top_p, O + te + terr);
       const int n = cnt;
       if (n <= kCap) {
-        // the candidates largest first: ranked in place of a sort when at most kTT
-        float* sc = cand;
-        if (n <= kTT) {
-          sc = cand + kCap / 2;
-          rank_sort(cand, n, sc);
-        } else {
+        // more than kTT candidates: sorted, largest first (at most kTT: reach_small takes them as they are)
+        const bool small = n <= kTT;
+        unsigned long long* wbuf = reinterpret_cast<unsigned long long*>(cand + kCap / 2);
+        if (!small) {
           int n2 = 1;
           while (n2 < n) n2 <<= 1;
           for (int i = n + tid; i < n2; i += kTT) cand[i] = -INFINITY;
@@ -762,10 +786,18 @@ __global__ void __launch_bounds__(kTT, 3) threshold_kernel(const void* __restric
             return;
           }
         } else if (nlo > O + ahi) {  // past the logits above the interval, whatever the exact sums
-          const Reach r = reach_two<kCap / kTT>(sc, n, nlo - O - ahi, nhi - O - alo, units, wsum, &rc);
-          if (r.a >= 0 && r.b >= 0 && sc[r.a] == sc[r.b]) {
-            if (tid == 0) thr[blockIdx.x] = sc[r.a];
-            return;
+          if (small) {
+            const Reached r = reach_small(cand, n, nlo - O - ahi, nhi - O - alo, units, wbuf, &rs);
+            if (r.found_a && r.found_b && r.a == r.b) {
+              if (tid == 0) thr[blockIdx.x] = r.a;
+              return;
+            }
+          } else {
+            const Reach r = reach_two<kCap / kTT>(cand, n, nlo - O - ahi, nhi - O - alo, units, wsum, &rc);
+            if (r.a >= 0 && r.b >= 0 && cand[r.a] == cand[r.b]) {
+              if (tid == 0) thr[blockIdx.x] = cand[r.a];
+              return;
+            }
           }
         }
         // undecided by the bounds: exact fixed-point sums over the same classes
@@ -786,10 +818,18 @@ __global__ void __launch_bounds__(kTT, 3) threshold_kernel(const void* __restric
           return;
         }
         if (need > O + ax) {
-          const Reach r = reach_two<kCap / kTT>(sc, n, need - O - ax, need - O - ax, units, wsum, &rc);
-          if (r.a >= 0) {
-            if (tid == 0) thr[blockIdx.x] = sc[r.a];
-            return;
+          if (small) {
+            const Reached r = reach_small(cand, n, need - O - ax, need - O - ax, units, wbuf, &rs);
+            if (r.found_a) {
+              if (tid == 0) thr[blockIdx.x] = r.a;
+              return;
+            }
+          } else {
+            const Reach r = reach_two<kCap / kTT>(cand, n, need - O - ax, need - O - ax, units, wsum, &rc);
+            if (r.a >= 0) {
+              if (tid == 0) thr[blockIdx.x] = cand[r.a];
+              return;
+            }
           }
         }
       }
