@@ -343,7 +343,7 @@ __device__ int first_reaching(const float* s, int n, unsigned long long need, U&
 // Among n <= kTT gathered logits (in any order): the logit at which the running sum of units, taken from the
 // largest down (ties by index), first reaches need_a, and the one for need_b.  Thread t sums the units
 // of the logits that come before cand[t] in that order, so no sort or scan is needed; w holds the units
-// (kTT slots).  found[k] = 0 if the whole sum stays below the need.  Every thread gets the results.
+// (kTT slots).  found_a / found_b = 0 if the whole sum stays below the need.  Every thread gets the results.
 struct Reached {
   float a, b;
   int found_a, found_b;
@@ -583,12 +583,13 @@ __device__ Bracket nucleus_bracket(const Hist& h, unsigned long long base, float
 //     gathered (or, past kCap logits, the radix selection) gives the threshold.
 //   nucleus: a bin's count bounds its mass within about 1.6 %, so the counts bracket the bins the running
 //     mass top_p * total can end in; pass 2 gathers the logits of a logit interval holding those bins and
-//     sums every weight in float: the total, and the mass above the interval.  The candidates' exact fixed-point weights are then scanned, in descending
-//     order, for the running mass top_p * total taken at both ends of the sums' error bounds: if both ends
-//     stop at the same logit, that logit is the threshold the exact fixed-point sums give; otherwise
-//     (rare: 1 or 2 of 1536 c3 rows) a pass of exact fixed-point sums decides.  A bracket of more than
-//     kCap logits (top_p within a few percent of 1) takes the weighted histogram instead: exact
-//     fixed-point masses per bin, then the gather.
+//     sums every weight in float: the total, and the mass above the interval.  Each candidate's exact
+//     fixed-point weight, with those of the candidates ranked above it, then locates the running mass
+//     top_p * total taken at both ends of the sums' error bounds: if both ends stop at the same logit,
+//     that logit is the threshold the exact fixed-point sums give; otherwise (rare: 5 to 7 of 1280-1536
+//     c3 rows) a pass of exact fixed-point sums decides.  A bracket of more than kCap logits (top_p
+//     within a few percent of 1) takes the weighted histogram instead: exact fixed-point masses per bin,
+//     then the gather.
 // So a long row is read twice, apart from its prefix and those fallbacks.  If more than kOver logits lie
 // above R, or the nucleus weights of the overflow could leave the fixed point (M - R above kOverUnits),
 // pass 1 is run again against R = M, where nothing lies above the reference.
